@@ -1,0 +1,274 @@
+"""Plain CPU oracle of the hybrid long-context attention path (SWA + CSA / SWA + HCA).
+
+TEST INFRASTRUCTURE ONLY.  Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU
+baseline of ``bench.py`` may import this module.  The CUDA library never calls it,
+and it shares no code with the CUDA library: it imports numpy and the standard
+library, nothing else.
+
+Every function works on ONE sequence, in float64, on numpy arrays indexed by
+absolute token position (no ring buffers, no blocking, no fusion).  Inputs may be
+float32 or bfloat16-valued arrays; they are widened to float64 exactly.
+
+Sources (web pages about DeepSeek-V4; none prints a formula, they give the data
+flow and the constants):
+  [V4-notes]  "DeepSeek-V4 深度研究剖析" (group-reading-wiki, DeepSeek-V4 research notes),
+              §5.2 SWA (n_win = 128 uncompressed KV), §5.3 CSA (every m = 4 tokens'
+              KV compressed into one entry; a Lightning Indexer scores the compressed
+              entries and the top-k are attended; k = 512 Flash / 1024 Pro),
+              §5.4 HCA (every m' = 128 tokens compressed into one entry, all
+              attended densely), §5.5 (the three paths as one memory hierarchy),
+              §8 (precision), §11.3 (deterministic kernels), §11.4 (cache kinds).
+  [LateTalk]  "163: DeepSeek V4 Explained: The Infra Whale, 1M-Token Context Made
+              Real, and Extreme Efficiency Optimization" (zjai.club), §14 (every
+              layer is SWA plus one of CSA / HCA, fixed per layer; MQA-style shared KV).
+  [EP95]      "EP 95 解读 DeepSeek-V4 论文" (aifrontier.kr), segment "处理 KV cache 的
+              Lightning Indexer 与 top-k 选择" (compress first, the indexer looks at
+              every compressed entry, take the top k, attend only to those) and the
+              description of the attention-block figure (the uncompressed window and
+              the compressed entries are concatenated before one MQA).
+
+The pages leave the compressor and the indexer open.  The definitions used here
+(and on the GPU) are:
+  compressor : per block, softmax over the block's m scalar gate logits, then the
+               gate-weighted sum of the block's rows (K, V and the indexer keys).
+  indexer    : s_j = sum_h w_h * max(0, qI_h . cI_j).
+Readings where the pages are silent (all listed with reasons in the design notes
+of the repository):
+  * eligibility: a compressed entry j is visible to the query at position t only
+    when its whole block lies before the window ("disjoint"):
+    n_elig(t) = floor(max(0, t + 1 - n_win) / m); the alternative "overlap" rule
+    floor((t + 1) / m) is available as a flag.
+  * the window of query t is the n_win positions max(0, t-n_win+1) .. t.
+  * the window keys and the attended compressed entries share one softmax.
+  * softmax scale 1/sqrt(d) over all d dims unless given.
+  * top-k order: score descending, then smaller index; NaN scores rank as -inf;
+    the result is emitted in ascending index order, padded with -1.
+  * a query with no key at all (context 0) gives o = 0 and lse = -inf.
+  * compressed entries are rounded to the storage type (round-to-nearest-even to
+    bfloat16, or to float32) because the cache stores them in that type.
+"""
+from __future__ import annotations
+
+import math
+
+import numpy as np
+
+__all__ = [
+    "round_to_bf16", "round_to_storage", "gate_softmax", "compress_block",
+    "compress", "n_eligible", "window_positions", "index_scores", "topk_select",
+    "attend", "merge_partials", "csa_decode", "hca_decode", "prefill_query",
+]
+
+
+# --------------------------------------------------------------------------
+# storage rounding ([V4-notes] §8: the KV cache is stored in a narrow type)
+# --------------------------------------------------------------------------
+def round_to_bf16(x):
+    """Round float64 values to the nearest bfloat16 value, ties to even.
+
+    bfloat16 keeps 8 significant bits (1 implicit + 7 stored) and float32's
+    exponent range.  Written directly on the float64 value (no float32 step, which
+    would round twice).  Values below the bfloat16 normal range are not expected
+    here and are rounded with the same 8-bit rule (no subnormal handling).
+    """
+    x = np.asarray(x, dtype=np.float64)
+    mant, expo = np.frexp(x)                     # x = mant * 2**expo, |mant| in [0.5, 1)
+    q = np.rint(np.ldexp(mant, 8))               # 8 significant bits, rint = ties-to-even
+    return np.ldexp(q, expo - 8)
+
+
+def round_to_storage(x, storage: str):
+    """Round to the cache storage type: 'bf16' or 'f32'."""
+    if storage == "bf16":
+        return round_to_bf16(x)
+    if storage == "f32":
+        return np.asarray(x, dtype=np.float64).astype(np.float32).astype(np.float64)
+    raise ValueError(f"unknown storage type {storage!r}")
+
+
+# --------------------------------------------------------------------------
+# a1 / a2: the token compressor ([V4-notes] §5.3 CSA m=4, §5.4 HCA m'=128)
+# --------------------------------------------------------------------------
+def gate_softmax(g):
+    """Softmax of one block's m gate logits (max-subtracted, float64)."""
+    g = np.asarray(g, dtype=np.float64)
+    e = np.exp(g - g.max())
+    return e / e.sum()
+
+
+def compress_block(rows, g):
+    """One compressed entry: sum_i alpha_i * rows[i], alpha = softmax(g) over the block."""
+    alpha = gate_softmax(g)
+    return alpha @ np.asarray(rows, dtype=np.float64)
+
+
+def compress(X, gate, m: int, j_begin: int, n_blk: int, storage: str | None = None):
+    """Compress blocks j_begin .. j_begin+n_blk-1 of a per-token array X [L, dX].
+
+    Block j covers positions j*m .. j*m+m-1 and must be complete.  Returns
+    [n_blk, dX]; rounded to ``storage`` when given.
+    """
+    X = np.asarray(X)
+    gate = np.asarray(gate)
+    out = np.empty((n_blk, X.shape[1]), dtype=np.float64)
+    for b in range(n_blk):
+        j = j_begin + b
+        lo, hi = j * m, (j + 1) * m
+        if hi > X.shape[0]:
+            raise ValueError(f"block {j} is not complete")
+        out[b] = compress_block(X[lo:hi], gate[lo:hi])
+    return out if storage is None else round_to_storage(out, storage)
+
+
+# --------------------------------------------------------------------------
+# what a query at position t sees ([V4-notes] §5.2, §5.3, §5.4)
+# --------------------------------------------------------------------------
+def n_eligible(t: int, n_win: int, m: int, rule: str = "disjoint") -> int:
+    """Number of compressed entries (0 .. n-1) visible to the query at position t."""
+    if rule == "disjoint":
+        return max(0, t + 1 - n_win) // m
+    if rule == "overlap":
+        return (t + 1) // m
+    raise ValueError(rule)
+
+
+def window_positions(t: int, n_win: int) -> np.ndarray:
+    """Positions of the uncompressed sliding window of the query at position t."""
+    return np.arange(max(0, t - n_win + 1), t + 1, dtype=np.int64)
+
+
+# --------------------------------------------------------------------------
+# a3: Lightning Indexer score ([V4-notes] §5.3; [EP95] indexer segment)
+# --------------------------------------------------------------------------
+def index_scores(qI, w, cI):
+    """s_j = sum_h w_h * max(0, qI_h . cI_j) for every row j of cI.
+
+    qI [H_I, d_I], w [H_I], cI [n, d_I] -> [n] float64.
+    """
+    qI = np.asarray(qI, dtype=np.float64)
+    w = np.asarray(w, dtype=np.float64)
+    cI = np.asarray(cI, dtype=np.float64)
+    dots = cI @ qI.T                              # [n, H_I]
+    return np.maximum(dots, 0.0) @ w
+
+
+# --------------------------------------------------------------------------
+# a4: top-k selection ([V4-notes] §5.3: k = 512 / 1024)
+# --------------------------------------------------------------------------
+def topk_select(scores, k: int) -> np.ndarray:
+    """Indices of the k best scores, best = larger score, then smaller index.
+
+    All entries are taken when there are at most k.  NaN ranks as -inf.
+    Returns int64 [k] in ascending index order, padded with -1.
+    """
+    s = np.asarray(scores, dtype=np.float64).copy()
+    s[np.isnan(s)] = -np.inf
+    n = s.shape[0]
+    take = min(k, n)
+    order = np.lexsort((np.arange(n), -s))        # primary key -s, then the index
+    chosen = np.sort(order[:take].astype(np.int64))
+    out = np.full(k, -1, dtype=np.int64)
+    out[:take] = chosen
+    return out
+
+
+# --------------------------------------------------------------------------
+# a5 / a6: joint attention and the split merge ([EP95] figure description:
+# window and compressed entries concatenated before one multi-query attention)
+# --------------------------------------------------------------------------
+def attend(q, keys, values, scale: float):
+    """Multi-query attention of H query heads over one shared set of keys.
+
+    q [H, d], keys [n, d], values [n, dv] -> (o [H, dv], lse [H]) with
+    z = scale * q.key, p = softmax(z) over the n keys, o = sum p * value,
+    lse = log sum exp z.  n = 0 gives o = 0, lse = -inf.
+    """
+    q = np.asarray(q, dtype=np.float64)
+    keys = np.asarray(keys, dtype=np.float64)
+    values = np.asarray(values, dtype=np.float64)
+    H = q.shape[0]
+    if keys.shape[0] == 0:
+        return np.zeros((H, values.shape[1])), np.full(H, -np.inf)
+    z = scale * (q @ keys.T)                      # [H, n]
+    zmax = z.max(axis=1, keepdims=True)
+    e = np.exp(z - zmax)
+    denom = e.sum(axis=1, keepdims=True)
+    p = e / denom
+    return p @ values, (zmax + np.log(denom))[:, 0]
+
+
+def merge_partials(o_parts, lse_parts):
+    """Combine attention results over disjoint key subsets.
+
+    o_parts [S, H, dv], lse_parts [S, H]:  LSE = log sum_s exp(lse_s),
+    o = sum_s exp(lse_s - LSE) * o_s.  Parts with lse = -inf carry no weight.
+    """
+    o_parts = np.asarray(o_parts, dtype=np.float64)
+    lse_parts = np.asarray(lse_parts, dtype=np.float64)
+    mx = lse_parts.max(axis=0)
+    H = lse_parts.shape[1]
+    o = np.zeros(o_parts.shape[1:])
+    lse = np.full(H, -np.inf)
+    for h in range(H):
+        if not np.isfinite(mx[h]):
+            continue
+        wgt = np.exp(lse_parts[:, h] - mx[h])
+        tot = wgt.sum()
+        lse[h] = mx[h] + math.log(tot)
+        o[h] = (wgt / tot) @ o_parts[:, h, :]
+    return o, lse
+
+
+def _joint_keys(comp_idx, ck, cv, k_tok, v_tok, t, n_win):
+    win = window_positions(t, n_win)
+    comp_idx = np.asarray(comp_idx, dtype=np.int64)
+    keys = np.concatenate([np.asarray(ck, np.float64)[comp_idx].reshape(-1, k_tok.shape[1]),
+                           np.asarray(k_tok, np.float64)[win]], axis=0)
+    vals = np.concatenate([np.asarray(cv, np.float64)[comp_idx].reshape(-1, v_tok.shape[1]),
+                           np.asarray(v_tok, np.float64)[win]], axis=0)
+    return keys, vals
+
+
+# --------------------------------------------------------------------------
+# one layer for one query, in the pages' order: compress -> index -> top-k -> attend
+# --------------------------------------------------------------------------
+def csa_decode(q, qI, w, ck, cv, cI, k_tok, v_tok, t: int, *, n_win: int, m: int, k: int,
+               scale: float, rule: str = "disjoint"):
+    """SWA + CSA for the query at position t of one sequence.
+
+    ck, cv, cI: the compressed caches (entries 0 .. n-1, already in storage type);
+    k_tok, v_tok: per-token K, V indexed by absolute position (at least t+1 rows).
+    Returns (o [H, dv], lse [H], idx [k] ascending with -1 padding, scores [n_elig]).
+    """
+    ne = n_eligible(t, n_win, m, rule)
+    scores = index_scores(qI, w, np.asarray(cI)[:ne])
+    idx = topk_select(scores, k)
+    sel = idx[idx >= 0]
+    keys, vals = _joint_keys(sel, ck, cv, k_tok, v_tok, t, n_win)
+    o, lse = attend(q, keys, vals, scale)
+    return o, lse, idx, scores
+
+
+def hca_decode(q, ck, cv, k_tok, v_tok, t: int, *, n_win: int, m: int, scale: float,
+               rule: str = "disjoint"):
+    """SWA + HCA for the query at position t: every eligible entry plus the window."""
+    ne = n_eligible(t, n_win, m, rule)
+    keys, vals = _joint_keys(np.arange(ne), ck, cv, k_tok, v_tok, t, n_win)
+    return attend(q, keys, vals, scale)
+
+
+def prefill_query(q, idx, ck, cv, k_tok, v_tok, t: int, *, n_win: int, m: int, scale: float,
+                  rule: str = "disjoint"):
+    """Attention of one prefill query at position t.
+
+    idx: this query's selected entries (CSA, -1 padded) or None for HCA (all
+    eligible entries).  Positions between the last eligible block and the window
+    start are not attended (the window stays exactly n_win wide).
+    """
+    if idx is None:
+        sel = np.arange(n_eligible(t, n_win, m, rule))
+    else:
+        idx = np.asarray(idx, dtype=np.int64)
+        sel = idx[idx >= 0]
+    keys, vals = _joint_keys(sel, ck, cv, k_tok, v_tok, t, n_win)
+    return attend(q, keys, vals, scale)
