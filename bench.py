@@ -1,0 +1,433 @@
+#!/usr/bin/env python3
+"""Decode throughput of one hybrid-attention layer on B300, printed as one JSON line.
+
+Default workload: CSA decode, 32 sequences at 65,536 tokens, 64 query heads of
+dim 512 on one shared K/V head, window 128, m = 4 (16,384 entries per
+sequence), top-512, indexer 64 heads x 128, bfloat16 storage, fp32 accumulation.
+One step = one decode token per sequence through the whole path: compress the
+block completed by the newest token, score every eligible entry, select the
+top-k, attend to selection + window (split-KV + merge).  The step's launches are
+captured once in a CUDA graph and replayed; timing uses CUDA events recorded
+inside the graph on the launching stream, with an L2 flush (256 MiB write)
+between timed steps.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+With N > 1 (torchrun, one process per GPU) every rank runs its own replica of
+the workload (weak scaling, no collective on the data path); the timed region is
+bracketed by barriers and the maximum over ranks is reported.
+`--impl reference` times the CPU oracle on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import re
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default="csa_decode_64k")
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    return ap.parse_args()
+
+
+# ----------------------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi sampling of SM clock and throttle reasons during the timed region."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = os.path.join("/tmp", f"ha_clocks_{os.getpid()}.csv")
+
+    def __enter__(self):
+        try:
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=self.fh, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.fh.close()
+
+    def summary(self):
+        if self.proc is None or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        os.unlink(self.path)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------- helpers
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        d = json.load(open(path))
+        return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
+                "bf16_tflops_sustained": d.get("bf16_tflops_sustained"), "source": "measured"}
+    return {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0,
+            "source": "fallback"}
+
+
+def profiled_traffic(kernel_name: str, source_file: str):
+    """DRAM bytes per launch of `kernel_name` from the committed ncu summary, or None
+    when there is none or the kernel's source changed since the capture."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.md")
+    if not os.path.exists(path):
+        return None
+    src = os.path.join(ROOT, "long_context_hybrid_02_b300", "csrc", source_file)
+    sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    for line in open(path):
+        m = re.match(r"\|\s*(\S+)\s*\|\s*(\S+)\s*\|\s*([0-9.eE+]+)\s*\|\s*([0-9a-f]{16})\s*\|", line)
+        if m and m.group(1) == kernel_name and m.group(4) == sha:
+            return float(m.group(3))
+    return None
+
+
+def step_bytes(w, n_elig: int, n_keys_win: int):
+    es = 2 if w.dtype == "bf16" else 4
+    out = {}
+    if w.kind == "csa":
+        out["compress"] = w.B * (w.m * (2 * w.d + w.d_I) * es + w.m * 4 + (2 * w.d + w.d_I) * es)
+        out["index"] = w.B * (n_elig * w.d_I * es + n_elig * 4 + w.H_I * w.d_I * es + w.H_I * 4)
+        out["topk"] = w.B * (n_elig * 4 + w.k * 4)
+        keys = min(w.k, n_elig) + n_keys_win
+        out["attention"] = w.B * (keys * 2 * w.d * es + 2 * w.H * w.d * es + w.k * 4)
+    else:
+        out["compress"] = w.B * (w.m * 2 * w.d * es + w.m * 4 + 2 * w.d * es)
+        keys = n_elig + n_keys_win
+        out["attention"] = w.B * (keys * 2 * w.d * es + 2 * w.H * w.d * es)
+    return out
+
+
+# ----------------------------------------------------------------------------- CPU oracle
+def oracle_sample(w, tok_host, qry_host, n_seq: int, seconds: float):
+    """Run the oracle decode step on sequences of the workload until `seconds` pass.
+
+    Returns (sequences decoded, wall seconds, threads).  The compressed caches of
+    the sampled sequences are built by the oracle itself before timing.
+    """
+    import numpy as np
+    import oracle as O
+    from threadpoolctl import threadpool_info
+
+    def f64(t):
+        return t.to("cpu").float().numpy().astype(np.float64)
+
+    caches = []
+    t = w.L - 1
+    ne = O.n_eligible(t, w.n_win, w.m)
+    for b in range(n_seq):
+        g = tok_host["gate"][b].numpy().astype(np.float64)
+        K = f64(tok_host["k_tok"][b])
+        V = f64(tok_host["v_tok"][b])
+        c = {"K": K, "V": V,
+             "ck": O.compress(K, g, w.m, 0, w.n_blocks, w.dtype),
+             "cv": O.compress(V, g, w.m, 0, w.n_blocks, w.dtype)}
+        if w.kind == "csa":
+            c["cki"] = O.compress(f64(tok_host["ki_tok"][b]), g, w.m, 0, w.n_blocks, w.dtype)
+        caches.append(c)
+    done, t0 = 0, time.perf_counter()
+    while True:
+        for b, c in enumerate(caches):
+            q = f64(qry_host["q"][b, 0])
+            if w.kind == "csa":
+                O.csa_decode(q, f64(qry_host["qI"][b, 0]), f64(qry_host["w_idx"][b, 0]), c["ck"],
+                             c["cv"], c["cki"], c["K"], c["V"], t, n_win=w.n_win, m=w.m, k=w.k,
+                             scale=1 / math.sqrt(w.d))
+            else:
+                O.hca_decode(q, c["ck"], c["cv"], c["K"], c["V"], t, n_win=w.n_win, m=w.m,
+                             scale=1 / math.sqrt(w.d))
+            done += 1
+        if time.perf_counter() - t0 >= seconds:
+            break
+    el = time.perf_counter() - t0
+    threads = max([d.get("num_threads", 1) for d in threadpool_info()] + [1])
+    return done, el, threads, ne
+
+
+def host_inputs(w, seqs: int):
+    """The workload's inputs for the first `seqs` sequences, drawn on the host."""
+    from long_context_hybrid_02_b300 import synth
+    ws = w.scaled(B=seqs)
+    return synth.make_tokens(ws, "cpu"), synth.make_queries(ws, "cpu")
+
+
+def run_reference(args, rank):
+    if rank != 0:
+        return
+    from long_context_hybrid_02_b300 import synth
+    w = synth.WORKLOADS[args.workload]
+    tok, qry = host_inputs(w, 1)
+    per_step = max(0.5, min(5.0, 120.0 / max(1, args.steps + args.warmup)))
+    for _ in range(args.warmup):
+        oracle_sample(w, tok, qry, 1, 0.0)
+    done, el = 0, 0.0
+    for _ in range(args.steps):
+        d, e, threads, _ = oracle_sample(w, tok, qry, 1, per_step)
+        done += d
+        el += e
+    value = done / el
+    cores = len(os.sched_getaffinity(0))
+    line = {"impl": "reference", "metric": "decode tokens/s (one layer, all sequences)",
+            "value": value, "unit": "tokens/s", "n_gpus": args.gpus, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": 1e3 * el / max(1, done),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded Gaussian, host-drawn)",
+            "config": {"workload": w.name, "B": w.B, "ctx": w.L, "H": w.H, "d": w.d,
+                       "n_win": w.n_win, "m": w.m, "k": w.k if w.kind == "csa" else None},
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+                             "host_cpus": cores,
+                             "sample": f"sequence 0 of the workload decoded repeatedly, "
+                                       f"{per_step:.1f}s per step"},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ----------------------------------------------------------------------------- GPU arm
+def main():
+    args = parse()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    import torch
+    import torch.distributed as dist
+    if world > 1:
+        dist.init_process_group("nccl" if args.impl == "ours" else "gloo")
+    if args.impl == "reference":
+        run_reference(args, rank)
+        if world > 1:
+            dist.barrier()
+            dist.destroy_process_group()
+        return
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    from long_context_hybrid_02_b300 import binding as B
+    from long_context_hybrid_02_b300 import build as bld
+    from long_context_hybrid_02_b300 import synth
+    from long_context_hybrid_02_b300.pipeline import HybridLayer
+    if not os.path.exists(bld.LIB):
+        bld.build()
+    B.load_library()
+    w = synth.WORKLOADS[args.workload]
+    assert w.decode, "the benchmark times decode workloads"
+    tok = synth.make_tokens(w, dev)
+    qry = synth.make_queries(w, dev)
+    layer = HybridLayer(w, tok, dev)
+    layer.build_cache()
+    new_blk = torch.full((w.B,), (w.L // w.m) - 1 if w.L % w.m == 0 else -1, dtype=torch.int32,
+                         device=dev)
+    q = qry["q"][:, 0].contiguous()
+    stream = torch.cuda.Stream(device=dev)
+    ev = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(5)]
+    names = ["compress", "index", "topk", "attention"] if w.kind == "csa" else ["compress", "attention"]
+
+    def step():
+        s = stream.cuda_stream
+        ev[0].record(stream)
+        layer.compress(new_blk, 1, s)
+        ev[1].record(stream)
+        if w.kind == "csa":
+            B.csa_index_scores(layer.p, qry["qI"], qry["w_idx"], layer.cki, layer.n_cap,
+                               qry["q_pos"], 1, layer.scores, s)
+            ev[2].record(stream)
+            B.csa_topk(layer.p, layer.scores, layer.n_cap, qry["q_pos"], 1, layer.idx,
+                       (layer.ws.data_ptr(), layer.ws.numel()), s)
+            ev[3].record(stream)
+            idx = layer.idx
+        else:
+            idx = None
+        B.hybrid_attn_decode(layer.p, q, layer.ck, layer.cv, layer.n_cap, idx, tok["k_tok"],
+                             tok["v_tok"], layer.tok_cap, qry["ctx_len"], layer.o, layer.lse,
+                             (layer.ws.data_ptr(), layer.ws.numel()), s)
+        ev[4 if w.kind == "csa" else 2].record(stream)
+
+    n_ev = len(names) + 1
+    # eager warm-up (sets kernel attributes), then capture
+    with torch.cuda.stream(stream):
+        step()
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    c0 = B.ha_launch_count()
+    with torch.cuda.graph(graph, stream=stream):
+        step()
+    launches_per_step = B.ha_launch_count() - c0
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+
+    def timed(k):
+        per = [[0.0] * (n_ev - 1) for _ in range(k)]
+        tot = []
+        for i in range(k):
+            flush.fill_(i & 0xFF)
+            graph.replay()
+            torch.cuda.synchronize()
+            for j in range(n_ev - 1):
+                per[i][j] = ev[j].elapsed_time(ev[j + 1])
+            tot.append(ev[0].elapsed_time(ev[n_ev - 1]))
+        return tot, per
+
+    for _ in range(args.warmup):
+        graph.replay()
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clocks:
+        t_wall0 = time.perf_counter()
+        tot, per = timed(args.steps)
+        torch.cuda.synchronize()
+        t_wall = time.perf_counter() - t_wall0
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    step_ms = sum(tot) / len(tot)
+    t_max = torch.tensor([sum(tot)], dtype=torch.float64, device=dev)
+    if world > 1:
+        dist.all_reduce(t_max, op=dist.ReduceOp.MAX)
+    total_ms = float(t_max.item())
+    tokens = w.B * world * args.steps
+    value = tokens / (total_ms / 1e3)
+    kern_ms = {n: sum(p[j] for p in per) / len(per) for j, n in enumerate(names)}
+
+    # ---- roofline of the dominant kernel (largest share of the step)
+    ne = max(0, w.L - w.n_win) // w.m          # entries visible to the decode query
+    nbytes = step_bytes(w, ne, min(w.n_win, w.L))
+    dom = max(kern_ms, key=kern_ms.get)
+    pk = peaks()
+    achieved = nbytes[dom] / (kern_ms[dom] * 1e-3) / 1e9
+    src_of = {"compress": "compress.cu", "index": "indexer.cu", "topk": "topk.cu",
+              "attention": "attention.cu"}
+    traffic = profiled_traffic(dom, src_of[dom])
+    roofline = {"bound": "hbm", "kernel": dom, "achieved": round(achieved, 1),
+                "peak": pk["hbm_gbs"], "unit": "GB/s", "frac": round(achieved / pk["hbm_gbs"], 4),
+                "traffic": traffic, "algorithmic_bytes": nbytes[dom],
+                "peak_source": pk["source"] + " (MEASURED_PEAKS.json hbm_gbs)"}
+
+    # ---- end to end through the public API: pinned host inputs -> step -> host output
+    es = 2 if w.dtype == "bf16" else 4
+    h_in = {"q": torch.empty_like(q, device="cpu").pin_memory()}
+    d_in = {"q": q}
+    if w.kind == "csa":
+        for kname in ("qI", "w_idx"):
+            h_in[kname] = torch.empty_like(qry[kname], device="cpu").pin_memory()
+            d_in[kname] = qry[kname]
+    row = (w.L - 1) % layer.tok_cap
+    for kname in (("k_tok", "v_tok", "ki_tok") if w.kind == "csa" else ("k_tok", "v_tok")):
+        h_in["new_" + kname] = torch.empty_like(tok[kname][:, row], device="cpu").pin_memory()
+        d_in["new_" + kname] = tok[kname][:, row]
+    h_in["new_gate"] = torch.empty_like(tok["gate"][:, row], device="cpu").pin_memory()
+    d_in["new_gate"] = tok["gate"][:, row]
+    for kname in h_in:
+        h_in[kname].copy_(d_in[kname])
+    h_out = torch.empty_like(layer.o, device="cpu").pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in h_in.values())
+    d2h = h_out.numel() * h_out.element_size()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e2e_ms = []
+    for i in range(args.steps):
+        flush.fill_(i & 0xFF)
+        torch.cuda.synchronize()
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            for kname in h_in:
+                d_in[kname].copy_(h_in[kname], non_blocking=True)
+            graph.replay()
+            h_out.copy_(layer.o, non_blocking=True)
+            e1.record(stream)
+        e1.synchronize()
+        e2e_ms.append(e0.elapsed_time(e1))
+    e2e_t = torch.tensor([sum(e2e_ms)], dtype=torch.float64, device=dev)
+    if world > 1:
+        dist.all_reduce(e2e_t, op=dist.ReduceOp.MAX)
+    e2e_value = tokens / (float(e2e_t.item()) / 1e3)
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        n_seq = 2
+        tok_h = {k: v[:n_seq].to("cpu") for k, v in tok.items()}
+        qry_h = {k: v[:n_seq].to("cpu") for k, v in qry.items()}
+        done, el, threads, _ = oracle_sample(w, tok_h, qry_h, n_seq, args.cpu_seconds)
+        cpu = {"value": done / el, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+               "host_cpus": len(os.sched_getaffinity(0)),
+               "sample": f"{done} decode tokens: sequences 0..{n_seq - 1} of the same inputs "
+                         f"(host copies) decoded repeatedly for {el:.1f}s; caches built untimed"}
+
+    clk = clocks.summary()
+    line = {
+        "metric": "decode tokens/s (one layer, all sequences)",
+        "value": round(value, 1), "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(step_ms, 5), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if w.dtype == "bf16" else "f32",
+        "data": "synthetic (seeded Gaussian drawn on the device)",
+        "config": {"workload": w.name, "kind": w.kind, "B": w.B, "ctx": w.L, "H": w.H, "d": w.d,
+                   "n_win": w.n_win, "m": w.m, "k": w.k if w.kind == "csa" else None,
+                   "H_I": w.H_I if w.kind == "csa" else None,
+                   "d_I": w.d_I if w.kind == "csa" else None,
+                   "l2": "flushed (256 MiB write) before every timed step",
+                   "timing": "CUDA events inside a CUDA graph, per step"},
+        "clocks": clk,
+        "e2e": {"value": round(e2e_value, 1), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": int(launches_per_step) * args.steps,
+        "roofline": roofline,
+        "cpu_baseline": cpu,
+        "kernel_ms": {k: round(v, 5) for k, v in kern_ms.items()},
+        "step_algorithmic_gbs": round(sum(nbytes.values()) / (step_ms * 1e-3) / 1e9, 1),
+        "wall_s_timed": round(t_wall, 3),
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,209 @@
+/*
+ * hybrid_attn.h -- C ABI of libhybridattn.so: the hot path of hybrid long-context
+ * attention (sliding window + compressed sparse attention, or sliding window +
+ * heavily compressed attention) for one NVIDIA B300 (sm_103a).
+ *
+ * Sources (web pages about DeepSeek-V4; they give the data flow and the
+ * constants, not the formulas):
+ *   [V4-notes] "DeepSeek-V4 深度研究剖析" (group-reading-wiki, DeepSeek-V4 research notes):
+ *              §5.2 SWA keeps the last n_win = 128 uncompressed KV; §5.3 CSA
+ *              compresses every m = 4 tokens' KV into one entry, a Lightning
+ *              Indexer scores the entries and the top-k (512 / 1024) are attended;
+ *              §5.4 HCA compresses every m' = 128 tokens into one entry and attends
+ *              to all of them; §11.4 the cache kinds (compressed KV, indexer KV,
+ *              window state, tail tokens of unfinished blocks).
+ *   [LateTalk] "163: DeepSeek V4 Explained ..." (zjai.club) §14: every layer is the
+ *              window plus one of CSA / HCA, fixed per layer, on one shared
+ *              (MQA-style) KV head.
+ *   [EP95]     "EP 95 解读 DeepSeek-V4 论文" (aifrontier.kr), the Lightning Indexer /
+ *              top-k segment and the attention-block figure (window keys and
+ *              compressed entries concatenated before one MQA).
+ * Formulas the pages leave open and this library fixes:
+ *   compressor  C_j = sum_{i<m} alpha_i X[j*m+i], alpha = softmax(gate[j*m .. j*m+m-1])
+ *   indexer     s_{t,j} = sum_h w_{t,h} * max(0, qI_{t,h} . CI_j)
+ *   eligibility n_elig(t) = floor(max(0, t+1-n_win)/m)   (HA_ELIG_DISJOINT, default)
+ *               n_elig(t) = floor((t+1)/m)               (HA_ELIG_OVERLAP)
+ *   attention   one softmax over {selected (CSA) or all eligible (HCA) entries}
+ *               plus the window positions max(0,t-n_win+1) .. t, scale 1/sqrt(d).
+ *
+ * Conventions shared by every call
+ *   - Every pointer argument except `p` is DEVICE memory owned by the caller.
+ *     The library allocates nothing, keeps no state between calls and never
+ *     synchronises the host; all work is ordered on `stream` (0 = legacy default).
+ *   - Arrays are row-major with the last dimension contiguous.  "T" is the
+ *     storage type selected by p->dtype (float for HA_F32, bfloat16 for
+ *     HA_BF16).  Gates, indexer weights, scores and lse are always float32;
+ *     indices and positions are int32.
+ *   - Per-token caches are [B, tok_cap, dim]; token position u of sequence b is
+ *     at slot (u % tok_cap).  tok_cap = context length gives a flat cache, a
+ *     smaller tok_cap a ring (the caller keeps the window and the tail tokens of
+ *     blocks not yet compressed resident).
+ *   - Compressed caches are [B, n_cap, dim]; entry j of sequence b is at row j.
+ *   - Every pointer must be 16-byte aligned, d and d_I multiples of 8
+ *     (HA_ERR_MISALIGNED / HA_ERR_UNSUPPORTED otherwise).
+ *   - Arguments are checked on the host before any launch; on error nothing is
+ *     launched and ha_last_error() describes the failure.  A failed launch
+ *     returns HA_ERR_CUDA.  Faults of the caller's memory surface at the
+ *     caller's next synchronisation.  Nothing aborts or throws across the ABI.
+ *   - Results are deterministic: fixed reduction orders, no atomics on data.
+ *   - Device-side positions (blk_begin, q_pos, ctx_len, idx) are range-checked by
+ *     the kernels: a block or entry outside [0, n_cap) is skipped, never read or
+ *     written.
+ */
+#ifndef HYBRID_ATTN_H_
+#define HYBRID_ATTN_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* ha_stream_t; /* same handle as cudaStream_t */
+
+typedef enum {
+  HA_OK = 0,
+  HA_ERR_INVALID_ARG = 1, /* a size or pointer is out of range / NULL        */
+  HA_ERR_MISALIGNED = 2,  /* a pointer is not 16-byte aligned                */
+  HA_ERR_UNSUPPORTED = 3, /* a shape outside the limits below                */
+  HA_ERR_WORKSPACE = 4,   /* ws is NULL or smaller than ha_workspace_size()  */
+  HA_ERR_CUDA = 5         /* a CUDA runtime call or a launch failed          */
+} ha_status;
+
+typedef enum { HA_F32 = 0, HA_BF16 = 1 } ha_dtype;
+typedef enum { HA_ELIG_DISJOINT = 0, HA_ELIG_OVERLAP = 1 } ha_elig;
+typedef enum { HA_OP_TOPK = 0, HA_OP_DECODE = 1, HA_OP_PREFILL = 2 } ha_op;
+
+/* Layer description.  Limits: 1 <= B; 1 <= H <= 256; 8 <= d <= 1024, d % 8 == 0;
+ * 1 <= n_win <= 65536; 1 <= m <= 1024; 1 <= k <= 4096 (CSA); 1 <= H_I <= 128;
+ * 8 <= d_I <= 512, d_I % 8 == 0.  scale <= 0 selects 1/sqrt(d). */
+typedef struct {
+  int32_t B;     /* sequences in the batch                                   */
+  int32_t H;     /* query heads sharing the single K/V head                  */
+  int32_t d;     /* head dim of q, K, V and of the compressed entries        */
+  int32_t n_win; /* sliding-window length ([V4-notes] §5.2: 128)             */
+  int32_t m;     /* tokens per compressed entry (CSA 4, HCA 128)             */
+  int32_t k;     /* entries selected per query (CSA; 512 / 1024)             */
+  int32_t H_I;   /* indexer heads                                            */
+  int32_t d_I;   /* indexer head dim (also the indexer-key dim)              */
+  int32_t dtype; /* ha_dtype of every T array                                */
+  int32_t elig;  /* ha_elig                                                  */
+  float scale;   /* softmax scale of the attention                           */
+} ha_params;
+
+/* ---------------------------------------------------------------------------
+ * hca_compress_kv -- HCA token compressor ([V4-notes] §5.4: every m' = 128
+ * tokens' KV becomes one entry; formula: per-block softmax-gated sum).
+ *   k_tok, v_tok : T [B, tok_cap, d]      per-token K and V
+ *   gate         : float [B, tok_cap]     one gate logit per token
+ *   blk_begin    : int32 [B]              first block to compress per sequence
+ *   n_blk        : blocks per sequence (>= 0; 0 is a no-op)
+ *   ck, cv       : T [B, n_cap, d]        rows blk_begin[b] .. +n_blk-1 written
+ * Block j reads positions j*m .. j*m+m-1 (the caller guarantees they are
+ * resident in the per-token cache).  Only K and V; p->m is the block size.
+ * ------------------------------------------------------------------------- */
+ha_status hca_compress_kv(const ha_params* p, const void* k_tok, const void* v_tok,
+                          const float* gate, int32_t tok_cap, const int32_t* blk_begin,
+                          int32_t n_blk, void* ck, void* cv, int32_t n_cap,
+                          ha_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * csa_compress_kv -- CSA token compressor ([V4-notes] §5.3: every m = 4 tokens'
+ * KV becomes one entry; §11.4: the indexer keys are a compressed cache of their
+ * own).  As hca_compress_kv, plus the indexer keys, compressed with the same
+ * gates:
+ *   ki_tok : T [B, tok_cap, d_I]   cki : T [B, n_cap, d_I]
+ * ------------------------------------------------------------------------- */
+ha_status csa_compress_kv(const ha_params* p, const void* k_tok, const void* v_tok,
+                          const void* ki_tok, const float* gate, int32_t tok_cap,
+                          const int32_t* blk_begin, int32_t n_blk, void* ck, void* cv,
+                          void* cki, int32_t n_cap, ha_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * csa_index_scores -- Lightning Indexer ([V4-notes] §5.3; [EP95]: it scores
+ * every compressed entry, so it must be light):
+ *   s[b,t,j] = sum_h w[b,t,h] * max(0, q_idx[b,t,h,:] . cki[b,j,:])
+ *   q_idx  : T [B, Tq, H_I, d_I]      w_idx : float [B, Tq, H_I]
+ *   cki    : T [B, n_cap, d_I]        q_pos : int32 [B, Tq] absolute positions
+ *   scores : float [B, Tq, n_cap]     written for j < min(n_elig(q_pos), n_cap)
+ *            only; the rest of each row is left untouched.
+ * ------------------------------------------------------------------------- */
+ha_status csa_index_scores(const ha_params* p, const void* q_idx, const float* w_idx,
+                           const void* cki, int32_t n_cap, const int32_t* q_pos, int32_t Tq,
+                           float* scores, ha_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * csa_topk -- top-k selection of compressed entries ([V4-notes] §5.3: k = 512
+ * for V4-Flash, 1024 for V4-Pro).  Per row (b, t) over the n = min(n_elig(t),
+ * n_cap) eligible scores: the k best by (score descending, index ascending),
+ * NaN ranked as -inf; all n when n <= k.  Written in ascending index order,
+ * padded with -1:
+ *   idx : int32 [B, Tq, k]
+ *   ws  : device workspace of ha_workspace_size(p, HA_OP_TOPK, Tq, n_cap) bytes
+ *         (may be 0 bytes, then ws may be NULL).
+ * ------------------------------------------------------------------------- */
+ha_status csa_topk(const ha_params* p, const float* scores, int32_t n_cap,
+                   const int32_t* q_pos, int32_t Tq, int32_t* idx, void* ws, size_t ws_bytes,
+                   ha_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * hybrid_attn_decode -- one decode query per sequence at t = ctx_len[b]-1
+ * ([V4-notes] §5.2-§5.5; [EP95] figure: window and compressed entries in one
+ * MQA softmax).
+ *   q          : T [B, H, d]
+ *   ck, cv     : T [B, n_cap, d]       compressed K / V
+ *   idx        : int32 [B, k]  CSA: attended entries (any order; entries < 0 or
+ *                >= min(n_elig(t), n_cap) are ignored)
+ *                NULL         HCA: every entry j < min(n_elig(t), n_cap)
+ *   k_tok,v_tok: T [B, tok_cap, d]     window source, tok_cap >= n_win
+ *   ctx_len    : int32 [B]   context length including the query token;
+ *                <= 0 gives o = 0, lse = -inf for that sequence
+ *   o          : T [B, H, d]           lse : float [B, H] or NULL
+ *   ws         : ha_workspace_size(p, HA_OP_DECODE, 1, n_cap) bytes (split
+ *                partials: the key list is split across CTAs and merged in a
+ *                fixed order).
+ * ------------------------------------------------------------------------- */
+ha_status hybrid_attn_decode(const ha_params* p, const void* q, const void* ck, const void* cv,
+                             int32_t n_cap, const int32_t* idx, const void* k_tok,
+                             const void* v_tok, int32_t tok_cap, const int32_t* ctx_len,
+                             void* o, float* lse, void* ws, size_t ws_bytes,
+                             ha_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * hybrid_attn_prefill -- Tq queries per sequence at absolute positions q_pos,
+ * each with its own selected set and its own causal window (the chunk's own
+ * tokens must already be in the per-token cache).  Same definitions as decode:
+ *   q   : T [B, Tq, H, d]        q_pos : int32 [B, Tq]
+ *   idx : int32 [B, Tq, k] (CSA) or NULL (HCA)
+ *   o   : T [B, Tq, H, d]        lse   : float [B, Tq, H] or NULL
+ *   ws  : ha_workspace_size(p, HA_OP_PREFILL, Tq, n_cap) bytes
+ * ------------------------------------------------------------------------- */
+ha_status hybrid_attn_prefill(const ha_params* p, const void* q, const int32_t* q_pos,
+                              int32_t Tq, const void* ck, const void* cv, int32_t n_cap,
+                              const int32_t* idx, const void* k_tok, const void* v_tok,
+                              int32_t tok_cap, void* o, float* lse, void* ws, size_t ws_bytes,
+                              ha_stream_t stream);
+
+/* Workspace bytes for `op` (ha_op) with Tq queries per sequence and n_cap
+ * compressed entries; `is_csa` = idx will be non-NULL (decode / prefill). */
+ha_status ha_workspace_size(const ha_params* p, int32_t op, int32_t Tq, int32_t n_cap,
+                            int32_t is_csa, size_t* bytes);
+
+/* Static description of a status code. */
+const char* ha_status_string(ha_status s);
+
+/* Detail of the last failed call on this host thread ("" if none). */
+const char* ha_last_error(void);
+
+/* ABI version of this header (bumped on any signature change). */
+int32_t ha_abi_version(void);
+
+/* Kernel launches issued by this library in this process so far (accounting;
+ * launches recorded into a CUDA graph count once, at capture). */
+uint64_t ha_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* HYBRID_ATTN_H_ */

@@ -1,0 +1,322 @@
+// C ABI of libhybridattn.so: host-side argument checks, launch planning and
+// dispatch to the kernels.  Every entry point validates its arguments before any
+// CUDA call, launches on the caller's stream and returns without synchronising.
+#include <math.h>
+#include <stdarg.h>
+#include <stdio.h>
+
+#include <atomic>
+#include <mutex>
+
+#include "common.cuh"
+#include "hybrid_attn.h"
+#include "kernels.h"
+
+namespace ha {
+
+namespace {
+std::atomic<unsigned long long> g_launches{0};
+struct SmemGrant { const void* func; int device; size_t bytes; };
+SmemGrant g_grants[256];
+int g_n_grants = 0;
+std::mutex g_grant_mu;
+}  // namespace
+
+cudaError_t ensure_smem(const void* func, size_t bytes) {
+  if (bytes <= 48 * 1024) return cudaSuccess;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  std::lock_guard<std::mutex> lock(g_grant_mu);
+  for (int i = 0; i < g_n_grants; ++i)
+    if (g_grants[i].func == func && g_grants[i].device == dev) {
+      if (g_grants[i].bytes >= bytes) return cudaSuccess;
+      e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, int(bytes));
+      if (e == cudaSuccess) g_grants[i].bytes = bytes;
+      return e;
+    }
+  e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, int(bytes));
+  if (e == cudaSuccess && g_n_grants < 256) g_grants[g_n_grants++] = {func, dev, bytes};
+  return e;
+}
+
+cudaError_t launched(cudaError_t e) {
+  if (e == cudaSuccess) g_launches.fetch_add(1, std::memory_order_relaxed);
+  return e;
+}
+
+unsigned long long launch_count() { return g_launches.load(); }
+
+}  // namespace ha
+
+namespace {
+
+thread_local char g_last_error[512] = "";
+
+ha_status fail(ha_status s, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_last_error, sizeof(g_last_error), fmt, ap);
+  va_end(ap);
+  return s;
+}
+
+ha_status cuda_status(cudaError_t e, const char* what) {
+  if (e == cudaSuccess) return HA_OK;
+  return fail(HA_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+bool aligned16(const void* ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15u) == 0; }
+
+#define HA_REQUIRE(cond, code, ...) \
+  do {                              \
+    if (!(cond)) return fail(code, __VA_ARGS__); \
+  } while (0)
+
+#define HA_PTR(ptr)                                                                 \
+  do {                                                                              \
+    HA_REQUIRE((ptr) != nullptr, HA_ERR_INVALID_ARG, "%s is NULL", #ptr);           \
+    HA_REQUIRE(aligned16(ptr), HA_ERR_MISALIGNED, "%s is not 16-byte aligned", #ptr); \
+  } while (0)
+
+#define HA_OPT_PTR(ptr)                                                               \
+  do {                                                                                \
+    if ((ptr) != nullptr)                                                             \
+      HA_REQUIRE(aligned16(ptr), HA_ERR_MISALIGNED, "%s is not 16-byte aligned", #ptr); \
+  } while (0)
+
+ha_status check_params(const ha_params* p, bool need_attn, bool need_index) {
+  HA_REQUIRE(p != nullptr, HA_ERR_INVALID_ARG, "params is NULL");
+  HA_REQUIRE(p->dtype == HA_F32 || p->dtype == HA_BF16, HA_ERR_INVALID_ARG, "dtype %d", p->dtype);
+  HA_REQUIRE(p->elig == HA_ELIG_DISJOINT || p->elig == HA_ELIG_OVERLAP, HA_ERR_INVALID_ARG,
+             "elig %d", p->elig);
+  HA_REQUIRE(p->B >= 1, HA_ERR_INVALID_ARG, "B = %d", p->B);
+  HA_REQUIRE(p->m >= 1 && p->m <= 1024, HA_ERR_UNSUPPORTED, "m = %d (1..1024)", p->m);
+  HA_REQUIRE(p->n_win >= 1 && p->n_win <= 65536, HA_ERR_UNSUPPORTED, "n_win = %d", p->n_win);
+  HA_REQUIRE(p->d >= 8 && p->d <= 1024 && p->d % 8 == 0, HA_ERR_UNSUPPORTED,
+             "d = %d (8..1024, multiple of 8)", p->d);
+  if (need_attn) {
+    HA_REQUIRE(p->H >= 1 && p->H <= 256, HA_ERR_UNSUPPORTED, "H = %d (1..256)", p->H);
+    HA_REQUIRE(isfinite(p->scale), HA_ERR_INVALID_ARG, "scale is not finite");
+  }
+  if (need_index) {
+    HA_REQUIRE(p->H_I >= 1 && p->H_I <= 128, HA_ERR_UNSUPPORTED, "H_I = %d (1..128)", p->H_I);
+    HA_REQUIRE(p->d_I >= 8 && p->d_I <= 512 && p->d_I % 8 == 0, HA_ERR_UNSUPPORTED,
+               "d_I = %d (8..512, multiple of 8)", p->d_I);
+    HA_REQUIRE((size_t)p->H_I * p->d_I <= 32768, HA_ERR_UNSUPPORTED, "H_I * d_I = %d > 32768",
+               p->H_I * p->d_I);
+  }
+  return HA_OK;
+}
+
+ha_status check_k(const ha_params* p) {
+  HA_REQUIRE(p->k >= 1 && p->k <= 4096, HA_ERR_UNSUPPORTED, "k = %d (1..4096)", p->k);
+  return HA_OK;
+}
+
+int max_keys(const ha_params* p, int n_cap, bool is_csa) {
+  return (is_csa ? p->k : n_cap) + p->n_win;
+}
+
+ha_status compress_common(const ha_params* p, int n_tensors, const void* const* src,
+                          void* const* dst, const int* dims, const float* gate, int32_t tok_cap,
+                          const int32_t* blk_begin, int32_t n_blk, int32_t n_cap,
+                          ha_stream_t stream, bool csa) {
+  ha_status s = check_params(p, false, csa);
+  if (s != HA_OK) return s;
+  for (int i = 0; i < n_tensors; ++i) {
+    HA_REQUIRE(src[i] != nullptr && dst[i] != nullptr, HA_ERR_INVALID_ARG, "tensor %d is NULL", i);
+    HA_REQUIRE(aligned16(src[i]) && aligned16(dst[i]), HA_ERR_MISALIGNED,
+               "tensor %d is not 16-byte aligned", i);
+  }
+  HA_PTR(gate);
+  HA_PTR(blk_begin);
+  HA_REQUIRE(tok_cap >= p->m, HA_ERR_INVALID_ARG, "tok_cap = %d < m = %d", tok_cap, p->m);
+  HA_REQUIRE(n_blk >= 0, HA_ERR_INVALID_ARG, "n_blk = %d", n_blk);
+  HA_REQUIRE(n_cap >= 1, HA_ERR_INVALID_ARG, "n_cap = %d", n_cap);
+  HA_REQUIRE((long long)p->B * n_blk <= 0x7fffffffLL, HA_ERR_UNSUPPORTED, "B * n_blk too large");
+  if (n_blk == 0) return HA_OK;
+  return cuda_status(ha::launch_compress(*p, n_tensors, src, dst, dims, gate, blk_begin, n_blk,
+                                         tok_cap, n_cap, (cudaStream_t)stream),
+                     "compress launch");
+}
+
+}  // namespace
+
+extern "C" {
+
+int32_t ha_abi_version(void) { return 1; }
+
+uint64_t ha_launch_count(void) { return ha::launch_count(); }
+
+const char* ha_last_error(void) { return g_last_error; }
+
+const char* ha_status_string(ha_status s) {
+  switch (s) {
+    case HA_OK: return "ok";
+    case HA_ERR_INVALID_ARG: return "invalid argument";
+    case HA_ERR_MISALIGNED: return "pointer not 16-byte aligned";
+    case HA_ERR_UNSUPPORTED: return "shape outside the supported limits";
+    case HA_ERR_WORKSPACE: return "workspace missing or too small";
+    case HA_ERR_CUDA: return "CUDA error";
+  }
+  return "unknown status";
+}
+
+ha_status hca_compress_kv(const ha_params* p, const void* k_tok, const void* v_tok,
+                          const float* gate, int32_t tok_cap, const int32_t* blk_begin,
+                          int32_t n_blk, void* ck, void* cv, int32_t n_cap,
+                          ha_stream_t stream) {
+  g_last_error[0] = 0;
+  if (!p) return fail(HA_ERR_INVALID_ARG, "params is NULL");
+  const void* src[2] = {k_tok, v_tok};
+  void* dst[2] = {ck, cv};
+  const int dims[2] = {p->d, p->d};
+  return compress_common(p, 2, src, dst, dims, gate, tok_cap, blk_begin, n_blk, n_cap, stream,
+                         false);
+}
+
+ha_status csa_compress_kv(const ha_params* p, const void* k_tok, const void* v_tok,
+                          const void* ki_tok, const float* gate, int32_t tok_cap,
+                          const int32_t* blk_begin, int32_t n_blk, void* ck, void* cv,
+                          void* cki, int32_t n_cap, ha_stream_t stream) {
+  g_last_error[0] = 0;
+  if (!p) return fail(HA_ERR_INVALID_ARG, "params is NULL");
+  const void* src[3] = {k_tok, v_tok, ki_tok};
+  void* dst[3] = {ck, cv, cki};
+  const int dims[3] = {p->d, p->d, p->d_I};
+  return compress_common(p, 3, src, dst, dims, gate, tok_cap, blk_begin, n_blk, n_cap, stream,
+                         true);
+}
+
+ha_status csa_index_scores(const ha_params* p, const void* q_idx, const float* w_idx,
+                           const void* cki, int32_t n_cap, const int32_t* q_pos, int32_t Tq,
+                           float* scores, ha_stream_t stream) {
+  g_last_error[0] = 0;
+  ha_status s = check_params(p, false, true);
+  if (s != HA_OK) return s;
+  HA_PTR(q_idx);
+  HA_PTR(w_idx);
+  HA_PTR(cki);
+  HA_PTR(q_pos);
+  HA_PTR(scores);
+  HA_REQUIRE(n_cap >= 1, HA_ERR_INVALID_ARG, "n_cap = %d", n_cap);
+  HA_REQUIRE(Tq >= 1, HA_ERR_INVALID_ARG, "Tq = %d", Tq);
+  HA_REQUIRE((long long)p->B * Tq <= 0x7fffffffLL, HA_ERR_UNSUPPORTED, "B * Tq too large");
+  return cuda_status(ha::launch_index_scores_simt(*p, q_idx, w_idx, cki, n_cap, q_pos, Tq, scores,
+                                                  (cudaStream_t)stream),
+                     "index launch");
+}
+
+ha_status csa_topk(const ha_params* p, const float* scores, int32_t n_cap, const int32_t* q_pos,
+                   int32_t Tq, int32_t* idx, void* ws, size_t ws_bytes, ha_stream_t stream) {
+  g_last_error[0] = 0;
+  ha_status s = check_params(p, false, false);
+  if (s != HA_OK) return s;
+  s = check_k(p);
+  if (s != HA_OK) return s;
+  HA_PTR(scores);
+  HA_PTR(q_pos);
+  HA_PTR(idx);
+  HA_OPT_PTR(ws);
+  HA_REQUIRE(n_cap >= 1, HA_ERR_INVALID_ARG, "n_cap = %d", n_cap);
+  HA_REQUIRE(Tq >= 1, HA_ERR_INVALID_ARG, "Tq = %d", Tq);
+  HA_REQUIRE((long long)p->B * Tq <= 0x7fffffffLL, HA_ERR_UNSUPPORTED, "B * Tq too large");
+  const size_t need = ha::topk_workspace_bytes(*p, Tq, n_cap);
+  HA_REQUIRE(ws_bytes >= need && (need == 0 || ws != nullptr), HA_ERR_WORKSPACE,
+             "workspace %zu bytes < %zu", ws_bytes, need);
+  return cuda_status(ha::launch_topk(*p, scores, n_cap, q_pos, Tq, idx, ws, ws_bytes,
+                                     (cudaStream_t)stream),
+                     "top-k launch");
+}
+
+ha_status hybrid_attn_decode(const ha_params* p, const void* q, const void* ck, const void* cv,
+                             int32_t n_cap, const int32_t* idx, const void* k_tok,
+                             const void* v_tok, int32_t tok_cap, const int32_t* ctx_len,
+                             void* o, float* lse, void* ws, size_t ws_bytes,
+                             ha_stream_t stream) {
+  g_last_error[0] = 0;
+  ha_status s = check_params(p, true, false);
+  if (s != HA_OK) return s;
+  if (idx) {
+    s = check_k(p);
+    if (s != HA_OK) return s;
+  }
+  HA_PTR(q);
+  HA_PTR(ck);
+  HA_PTR(cv);
+  HA_OPT_PTR(idx);
+  HA_PTR(k_tok);
+  HA_PTR(v_tok);
+  HA_PTR(ctx_len);
+  HA_PTR(o);
+  HA_OPT_PTR(lse);
+  HA_OPT_PTR(ws);
+  HA_REQUIRE(n_cap >= 1, HA_ERR_INVALID_ARG, "n_cap = %d", n_cap);
+  HA_REQUIRE(tok_cap >= p->n_win, HA_ERR_INVALID_ARG, "tok_cap = %d < n_win = %d", tok_cap,
+             p->n_win);
+  const ha::AttnPlan pl = ha::plan_attention_simt(*p, p->B, max_keys(p, n_cap, idx != nullptr), true);
+  HA_REQUIRE(ws_bytes >= pl.ws_bytes && (pl.ws_bytes == 0 || ws != nullptr), HA_ERR_WORKSPACE,
+             "workspace %zu bytes < %zu", ws_bytes, pl.ws_bytes);
+  return cuda_status(ha::launch_attention_simt(*p, pl, 1, 1, q, ctx_len, ck, cv, n_cap, idx, k_tok,
+                                               v_tok, tok_cap, o, lse, ws, (cudaStream_t)stream),
+                     "decode launch");
+}
+
+ha_status hybrid_attn_prefill(const ha_params* p, const void* q, const int32_t* q_pos,
+                              int32_t Tq, const void* ck, const void* cv, int32_t n_cap,
+                              const int32_t* idx, const void* k_tok, const void* v_tok,
+                              int32_t tok_cap, void* o, float* lse, void* ws, size_t ws_bytes,
+                              ha_stream_t stream) {
+  g_last_error[0] = 0;
+  ha_status s = check_params(p, true, false);
+  if (s != HA_OK) return s;
+  if (idx) {
+    s = check_k(p);
+    if (s != HA_OK) return s;
+  }
+  HA_PTR(q);
+  HA_PTR(q_pos);
+  HA_PTR(ck);
+  HA_PTR(cv);
+  HA_OPT_PTR(idx);
+  HA_PTR(k_tok);
+  HA_PTR(v_tok);
+  HA_PTR(o);
+  HA_OPT_PTR(lse);
+  HA_OPT_PTR(ws);
+  HA_REQUIRE(n_cap >= 1, HA_ERR_INVALID_ARG, "n_cap = %d", n_cap);
+  HA_REQUIRE(Tq >= 1, HA_ERR_INVALID_ARG, "Tq = %d", Tq);
+  HA_REQUIRE((long long)p->B * Tq <= 0x7fffffffLL, HA_ERR_UNSUPPORTED, "B * Tq too large");
+  HA_REQUIRE(tok_cap >= p->n_win, HA_ERR_INVALID_ARG, "tok_cap = %d < n_win = %d", tok_cap,
+             p->n_win);
+  const ha::AttnPlan pl =
+      ha::plan_attention_simt(*p, p->B * Tq, max_keys(p, n_cap, idx != nullptr), false);
+  HA_REQUIRE(ws_bytes >= pl.ws_bytes && (pl.ws_bytes == 0 || ws != nullptr), HA_ERR_WORKSPACE,
+             "workspace %zu bytes < %zu", ws_bytes, pl.ws_bytes);
+  return cuda_status(ha::launch_attention_simt(*p, pl, 0, Tq, q, q_pos, ck, cv, n_cap, idx, k_tok,
+                                               v_tok, tok_cap, o, lse, ws, (cudaStream_t)stream),
+                     "prefill launch");
+}
+
+ha_status ha_workspace_size(const ha_params* p, int32_t op, int32_t Tq, int32_t n_cap,
+                            int32_t is_csa, size_t* bytes) {
+  g_last_error[0] = 0;
+  HA_REQUIRE(bytes != nullptr, HA_ERR_INVALID_ARG, "bytes is NULL");
+  *bytes = 0;
+  ha_status s = check_params(p, op != HA_OP_TOPK, false);
+  if (s != HA_OK) return s;
+  HA_REQUIRE(Tq >= 1 && n_cap >= 1, HA_ERR_INVALID_ARG, "Tq = %d, n_cap = %d", Tq, n_cap);
+  switch (op) {
+    case HA_OP_TOPK: *bytes = ha::topk_workspace_bytes(*p, Tq, n_cap); return HA_OK;
+    case HA_OP_DECODE:
+      *bytes = ha::plan_attention_simt(*p, p->B, max_keys(p, n_cap, is_csa != 0), true).ws_bytes;
+      return HA_OK;
+    case HA_OP_PREFILL:
+      *bytes = ha::plan_attention_simt(*p, p->B * Tq, max_keys(p, n_cap, is_csa != 0), false).ws_bytes;
+      return HA_OK;
+  }
+  return fail(HA_ERR_INVALID_ARG, "op = %d", op);
+}
+
+}  // extern "C"

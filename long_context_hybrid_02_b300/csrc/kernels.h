@@ -1,0 +1,42 @@
+// Internal launchers of the CUDA library (not part of the C ABI).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "hybrid_attn.h"
+
+namespace ha {
+
+// compress.cu: n_tensors row tensors compressed with the same gates.
+cudaError_t launch_compress(const ha_params& p, int n_tensors, const void* const* src,
+                            void* const* dst, const int* dims, const float* gate,
+                            const int32_t* blk_begin, int n_blk, int tok_cap, int n_cap,
+                            cudaStream_t st);
+
+// indexer.cu: CUDA-core indexer for every shape and type.
+cudaError_t launch_index_scores_simt(const ha_params& p, const void* q_idx, const float* w_idx,
+                                     const void* cki, int n_cap, const int32_t* q_pos, int Tq,
+                                     float* scores, cudaStream_t st);
+
+// topk.cu
+size_t topk_workspace_bytes(const ha_params& p, int Tq, int n_cap);
+cudaError_t launch_topk(const ha_params& p, const float* scores, int n_cap, const int32_t* q_pos,
+                        int Tq, int32_t* idx, void* ws, size_t ws_bytes, cudaStream_t st);
+
+// attention.cu: split-KV CUDA-core attention (decode and prefill) + merge.
+struct AttnPlan {
+  int n_splits;        // key-list ranges per query row
+  int keys_per_split;  // multiple of 32
+  int tile;            // keys staged per shared-memory tile
+  size_t ws_bytes;     // float32 partials when n_splits > 1
+};
+AttnPlan plan_attention_simt(const ha_params& p, int rows, int max_keys, bool decode);
+cudaError_t launch_attention_simt(const ha_params& p, const AttnPlan& pl, int decode, int Tq,
+                                  const void* q, const int32_t* pos, const void* ck,
+                                  const void* cv, int n_cap, const int32_t* idx,
+                                  const void* k_tok, const void* v_tok, int tok_cap, void* o,
+                                  float* lse, void* ws, cudaStream_t st);
+
+}  // namespace ha

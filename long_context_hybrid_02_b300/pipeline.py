@@ -1,0 +1,97 @@
+"""One hybrid-attention layer driven through the C ABI.
+
+`HybridLayer` owns the device buffers of one layer (compressed caches, scores,
+selected indices, outputs, workspace) and issues the library calls of a decode
+step or a prefill chunk in the order the method runs them: compress the block
+that just completed -> score every eligible entry -> select the top k -> attend
+to the selection plus the window (CSA); compress -> attend to every eligible
+entry plus the window (HCA).  Torch only allocates memory and provides the
+stream; every step runs in the library's CUDA kernels.
+"""
+from __future__ import annotations
+
+import torch
+
+from . import binding as B
+from .synth import Workload
+
+
+def params_for(w: Workload, Tq_override: int | None = None) -> B.Params:
+    return B.make_params(w.B, w.H, w.d, w.n_win, w.m, w.k if w.kind == "csa" else 1,
+                         w.H_I if w.kind == "csa" else 1, w.d_I if w.kind == "csa" else 8,
+                         B.F32 if w.dtype == "f32" else B.BF16, B.ELIG_DISJOINT, 0.0)
+
+
+class HybridLayer:
+    def __init__(self, w: Workload, tokens: dict, device="cuda", n_cap: int | None = None,
+                 tok_cap: int | None = None):
+        self.w = w
+        self.device = device
+        self.p = params_for(w)
+        self.csa = w.kind == "csa"
+        self.tok = tokens
+        self.tok_cap = tok_cap or tokens["k_tok"].shape[1]
+        self.n_cap = n_cap or w.n_blocks
+        dt = w.torch_dtype
+        self.ck = torch.empty((w.B, self.n_cap, w.d), dtype=dt, device=device)
+        self.cv = torch.empty((w.B, self.n_cap, w.d), dtype=dt, device=device)
+        self.cki = torch.empty((w.B, self.n_cap, w.d_I), dtype=dt, device=device) if self.csa else None
+        Tq = w.Tq
+        self.scores = torch.empty((w.B, Tq, self.n_cap), dtype=torch.float32, device=device) if self.csa else None
+        self.idx = torch.empty((w.B, Tq, w.k), dtype=torch.int32, device=device) if self.csa else None
+        self.o = torch.empty((w.B, Tq, w.H, w.d), dtype=dt, device=device)
+        self.lse = torch.empty((w.B, Tq, w.H), dtype=torch.float32, device=device)
+        op = B.OP_DECODE if w.decode else B.OP_PREFILL
+        nb = B.ha_workspace_size(self.p, op, Tq, self.n_cap, self.csa)
+        if self.csa:
+            nb = max(nb, B.ha_workspace_size(self.p, B.OP_TOPK, Tq, self.n_cap, True))
+        self.ws = torch.empty((max(nb, 16),), dtype=torch.uint8, device=device)
+        self.blk_zero = torch.zeros((w.B,), dtype=torch.int32, device=device)
+
+    # ------------------------------------------------------------------ caches
+    def compress(self, blk_begin: torch.Tensor, n_blk: int, stream=None):
+        t = self.tok
+        if self.csa:
+            B.csa_compress_kv(self.p, t["k_tok"], t["v_tok"], t["ki_tok"], t["gate"], self.tok_cap,
+                              blk_begin, n_blk, self.ck, self.cv, self.cki, self.n_cap, stream)
+        else:
+            B.hca_compress_kv(self.p, t["k_tok"], t["v_tok"], t["gate"], self.tok_cap, blk_begin,
+                              n_blk, self.ck, self.cv, self.n_cap, stream)
+
+    def build_cache(self, n_blk: int | None = None, stream=None):
+        """Compress blocks 0 .. n_blk-1 of every sequence (all complete blocks by default)."""
+        self.compress(self.blk_zero, self.n_cap if n_blk is None else n_blk, stream)
+
+    # ------------------------------------------------------------------ steps
+    def decode_step(self, q, ctx_len, new_blk, qI=None, w_idx=None, q_pos=None, stream=None):
+        """One decode token per sequence.
+
+        new_blk: int32 [B] index of the block completed by the newest token, or None
+        when no block completed at this step.  q_pos = ctx_len - 1 (int32 [B, 1]).
+        """
+        if new_blk is not None:
+            self.compress(new_blk, 1, stream)
+        ws = (self.ws.data_ptr(), self.ws.numel())
+        if self.csa:
+            B.csa_index_scores(self.p, qI, w_idx, self.cki, self.n_cap, q_pos, 1, self.scores, stream)
+            B.csa_topk(self.p, self.scores, self.n_cap, q_pos, 1, self.idx, ws, stream)
+            B.hybrid_attn_decode(self.p, q, self.ck, self.cv, self.n_cap, self.idx,
+                                 self.tok["k_tok"], self.tok["v_tok"], self.tok_cap, ctx_len,
+                                 self.o, self.lse, ws, stream)
+        else:
+            B.hybrid_attn_decode(self.p, q, self.ck, self.cv, self.n_cap, None, self.tok["k_tok"],
+                                 self.tok["v_tok"], self.tok_cap, ctx_len, self.o, self.lse, ws,
+                                 stream)
+        return self.o
+
+    def prefill_chunk(self, q, q_pos, qI=None, w_idx=None, stream=None):
+        """Tq queries per sequence (their tokens and blocks already in the caches)."""
+        Tq = q.shape[1]
+        ws = (self.ws.data_ptr(), self.ws.numel())
+        if self.csa:
+            B.csa_index_scores(self.p, qI, w_idx, self.cki, self.n_cap, q_pos, Tq, self.scores, stream)
+            B.csa_topk(self.p, self.scores, self.n_cap, q_pos, Tq, self.idx, ws, stream)
+        B.hybrid_attn_prefill(self.p, q, q_pos, Tq, self.ck, self.cv, self.n_cap,
+                              self.idx if self.csa else None, self.tok["k_tok"], self.tok["v_tok"],
+                              self.tok_cap, self.o, self.lse, ws, stream)
+        return self.o

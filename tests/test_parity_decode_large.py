@@ -1,0 +1,187 @@
+"""GPU vs oracle at the full decode workloads, in the benchmark's launch configuration.
+
+CSA decode: 32 sequences x 65,536 tokens, 64 heads x 512, RoPE on 64 dims,
+top-512 of 16,352 eligible entries, indexer 64 x 128, bfloat16.
+HCA decode: 32 sequences x 131,072 tokens, 64 heads x 512, 1,023 eligible entries.
+The oracle cannot redo the whole batch in seconds, so every stage is checked on
+sampled outputs, each computed by the oracle from the very same inputs:
+  * compression: sampled blocks of every tensor;
+  * indexer + top-k: generator-made compressed indexer keys fed to both sides,
+    full score rows and index sets of sampled sequences;
+  * top-k alone: oracle scores (float32) fed to both sides, exact index sets;
+  * attention alone: generator-made compressed K/V and the oracle's index sets;
+  * the whole decode step on sampled sequences, with caches the oracle builds
+    itself from the per-token inputs.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+from long_context_hybrid_02_b300 import binding as B
+from long_context_hybrid_02_b300 import synth
+from long_context_hybrid_02_b300.pipeline import HybridLayer
+from tests._harness import assert_close, assert_sorted_unique, assert_topk_match, np64
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+SAMPLE_SEQS = (0, 17, 31)
+
+
+@pytest.fixture(scope="module")
+def csa():
+    w = synth.WORKLOADS["csa_decode_64k"]
+    tok = synth.make_tokens(w, DEV)
+    qry = synth.make_queries(w, DEV)
+    layer = HybridLayer(w, tok, DEV)
+    layer.build_cache()
+    torch.cuda.synchronize()
+    yield w, tok, qry, layer
+    del layer, tok, qry
+    torch.cuda.empty_cache()
+
+
+def test_csa_compress_sampled_blocks(csa):
+    w, tok, qry, layer = csa
+    rng = np.random.default_rng(0)
+    for b in SAMPLE_SEQS:
+        for j in list(rng.integers(0, w.n_blocks, 20)) + [0, w.n_blocks - 1]:
+            rows = slice(j * w.m, (j + 1) * w.m)
+            g = np64(tok["gate"][b, rows])
+            for name, cname in (("k_tok", "ck"), ("v_tok", "cv"), ("ki_tok", "cki")):
+                ref = O.compress(np64(tok[name][b, rows]), g, w.m, 0, 1, "bf16")[0]
+                assert_close(np64(getattr(layer, cname)[b, j]), ref, "bf16", f"{cname}[{b},{j}]")
+
+
+def test_csa_index_and_topk_on_identical_keys(csa):
+    """Indexer over generator-made compressed keys: score rows within tolerance and
+    top-512 sets identical up to the 1e-6 band around the k-th oracle score."""
+    w, tok, qry, layer = csa
+    cki = synth.gaussian((w.B, w.n_blocks, w.d_I), DEV, 101, 1 / math.sqrt(w.d_I), torch.bfloat16)
+    B.csa_index_scores(layer.p, qry["qI"], qry["w_idx"], cki, layer.n_cap, qry["q_pos"], 1,
+                       layer.scores)
+    B.csa_topk(layer.p, layer.scores, layer.n_cap, qry["q_pos"], 1, layer.idx,
+               (layer.ws.data_ptr(), layer.ws.numel()))
+    torch.cuda.synchronize()
+    t = w.L - 1
+    ne = O.n_eligible(t, w.n_win, w.m)
+    for b in SAMPLE_SEQS:
+        ref = O.index_scores(np64(qry["qI"][b, 0]), np64(qry["w_idx"][b, 0]), np64(cki[b, :ne]))
+        got = np64(layer.scores[b, 0, :ne])
+        # float32 accumulation of bfloat16 products vs float64
+        np.testing.assert_allclose(got, ref, rtol=1e-5, atol=1e-6 * np.abs(ref).max())
+        gi = layer.idx[b, 0].cpu().numpy()
+        assert_sorted_unique(gi, ne, w.k, f"idx[{b}]")
+        assert_topk_match(gi, O.topk_select(ref, w.k), ref, w.k, f"top-k[{b}]")
+
+
+def test_csa_topk_exact_on_identical_scores(csa):
+    w, tok, qry, layer = csa
+    t = w.L - 1
+    ne = O.n_eligible(t, w.n_win, w.m)
+    g = torch.Generator().manual_seed(7)
+    s = torch.randn((w.B, 1, layer.n_cap), generator=g)
+    s[3, 0, :100] = float("nan")
+    s[5, 0, :] = torch.round(s[5, 0, :] * 4) / 4                    # heavy ties
+    sd = s.to(DEV)
+    idx = torch.empty_like(layer.idx)
+    B.csa_topk(layer.p, sd, layer.n_cap, qry["q_pos"], 1, idx, (layer.ws.data_ptr(), layer.ws.numel()))
+    torch.cuda.synchronize()
+    for b in (0, 3, 5, 31):
+        ref = O.topk_select(s[b, 0, :ne].double().numpy(), w.k)
+        assert idx[b, 0].cpu().numpy().tolist() == ref.tolist(), b
+
+
+def test_csa_attention_stage(csa):
+    """hybrid_attn_decode on generator-made compressed K/V and oracle index sets."""
+    w, tok, qry, layer = csa
+    ck = synth.gaussian((w.B, w.n_blocks, w.d), DEV, 201, 1 / math.sqrt(w.d), torch.bfloat16)
+    cv = synth.gaussian((w.B, w.n_blocks, w.d), DEV, 202, 1 / math.sqrt(w.d), torch.bfloat16)
+    t = w.L - 1
+    ne = O.n_eligible(t, w.n_win, w.m)
+    idx = synth.random_index_sets(w.B, 1, w.k, torch.full((w.B, 1), ne), DEV, 3)[:, 0].contiguous()
+    o = torch.empty((w.B, w.H, w.d), dtype=torch.bfloat16, device=DEV)
+    lse = torch.empty((w.B, w.H), dtype=torch.float32, device=DEV)
+    B.hybrid_attn_decode(layer.p, qry["q"][:, 0].contiguous(), ck, cv, layer.n_cap, idx,
+                         tok["k_tok"], tok["v_tok"], layer.tok_cap, qry["ctx_len"], o, lse,
+                         (layer.ws.data_ptr(), layer.ws.numel()))
+    torch.cuda.synchronize()
+    win = O.window_positions(t, w.n_win)
+    for b in SAMPLE_SEQS:
+        sel = idx[b].cpu().numpy()
+        keys = np.concatenate([np64(ck[b])[sel], np64(tok["k_tok"][b, win[0]:t + 1])])
+        vals = np.concatenate([np64(cv[b])[sel], np64(tok["v_tok"][b, win[0]:t + 1])])
+        ro, rl = O.attend(np64(qry["q"][b, 0]), keys, vals, 1 / math.sqrt(w.d))
+        assert_close(np64(o[b]), ro, "bf16", f"o[{b}]")
+        assert_close(np64(lse[b]), rl, "bf16", f"lse[{b}]")
+
+
+def test_csa_decode_step_end_to_end(csa):
+    """The benchmark's launch sequence; the oracle builds its own caches for two
+    sequences and runs compress -> index -> top-k -> attend in float64."""
+    w, tok, qry, layer = csa
+    new_blk = torch.full((w.B,), w.n_blocks - 1, dtype=torch.int32, device=DEV)
+    layer.decode_step(qry["q"][:, 0].contiguous(), qry["ctx_len"], new_blk, qry["qI"],
+                      qry["w_idx"], qry["q_pos"])
+    torch.cuda.synchronize()
+    t = w.L - 1
+    for b in (0, 31):
+        g = np64(tok["gate"][b])
+        K, V = np64(tok["k_tok"][b]), np64(tok["v_tok"][b])
+        ck = O.compress(K, g, w.m, 0, w.n_blocks, "bf16")
+        cv = O.compress(V, g, w.m, 0, w.n_blocks, "bf16")
+        cki = O.compress(np64(tok["ki_tok"][b]), g, w.m, 0, w.n_blocks, "bf16")
+        o, lse, idx, scores = O.csa_decode(np64(qry["q"][b, 0]), np64(qry["qI"][b, 0]),
+                                           np64(qry["w_idx"][b, 0]), ck, cv, cki, K, V, t,
+                                           n_win=w.n_win, m=w.m, k=w.k, scale=1 / math.sqrt(w.d))
+        gi = layer.idx[b, 0].cpu().numpy()
+        overlap = len(set(gi.tolist()) & set(idx.tolist())) / w.k
+        # the two sides' compressed indexer keys may differ by one bfloat16 unit in
+        # a few elements, which can swap entries right at the k-th score
+        assert overlap >= 0.99, overlap
+        assert_close(np64(layer.o[b, 0]), o, "bf16", f"o[{b}]")
+        assert_close(np64(layer.lse[b, 0]), lse, "bf16", f"lse[{b}]")
+
+
+@pytest.fixture(scope="module")
+def hca():
+    w = synth.WORKLOADS["hca_decode_128k"]
+    tok = synth.make_tokens(w, DEV)
+    qry = synth.make_queries(w, DEV)
+    layer = HybridLayer(w, tok, DEV)
+    layer.build_cache()
+    torch.cuda.synchronize()
+    yield w, tok, qry, layer
+    del layer, tok, qry
+    torch.cuda.empty_cache()
+
+
+def test_hca_compress_sampled_blocks(hca):
+    w, tok, qry, layer = hca
+    rng = np.random.default_rng(1)
+    for b in SAMPLE_SEQS:
+        for j in list(rng.integers(0, w.n_blocks, 8)) + [0, w.n_blocks - 1]:
+            rows = slice(j * w.m, (j + 1) * w.m)
+            g = np64(tok["gate"][b, rows])
+            for name, cname in (("k_tok", "ck"), ("v_tok", "cv")):
+                ref = O.compress(np64(tok[name][b, rows]), g, w.m, 0, 1, "bf16")[0]
+                assert_close(np64(getattr(layer, cname)[b, j]), ref, "bf16", f"{cname}[{b},{j}]")
+
+
+def test_hca_decode_step_end_to_end(hca):
+    w, tok, qry, layer = hca
+    new_blk = torch.full((w.B,), w.n_blocks - 1, dtype=torch.int32, device=DEV)
+    layer.decode_step(qry["q"][:, 0].contiguous(), qry["ctx_len"], new_blk, q_pos=qry["q_pos"])
+    torch.cuda.synchronize()
+    t = w.L - 1
+    for b in SAMPLE_SEQS:
+        g = np64(tok["gate"][b])
+        K, V = np64(tok["k_tok"][b]), np64(tok["v_tok"][b])
+        ck = O.compress(K, g, w.m, 0, w.n_blocks, "bf16")
+        cv = O.compress(V, g, w.m, 0, w.n_blocks, "bf16")
+        o, lse = O.hca_decode(np64(qry["q"][b, 0]), ck, cv, K, V, t, n_win=w.n_win, m=w.m,
+                              scale=1 / math.sqrt(w.d))
+        assert_close(np64(layer.o[b, 0]), o, "bf16", f"o[{b}]")
+        assert_close(np64(layer.lse[b, 0]), lse, "bf16", f"lse[{b}]")
