@@ -154,7 +154,6 @@ def oracle_sample(w, tok_host, qry_host, n_seq: int, seconds: float):
     """
     import numpy as np
     import oracle as O
-    from threadpoolctl import threadpool_info
 
     def f64(t):
         return t.to("cpu").float().numpy().astype(np.float64)
@@ -187,8 +186,19 @@ def oracle_sample(w, tok_host, qry_host, n_seq: int, seconds: float):
         if time.perf_counter() - t0 >= seconds:
             break
     el = time.perf_counter() - t0
-    threads = max([d.get("num_threads", 1) for d in threadpool_info()] + [1])
-    return done, el, threads, ne
+    return done, el, blas_threads(), ne
+
+
+def blas_threads() -> int:
+    """Threads numpy's BLAS may use (threadpoolctl when present, else the CPU affinity)."""
+    try:
+        from threadpoolctl import threadpool_info
+        return max([d.get("num_threads", 1) for d in threadpool_info()] + [1])
+    except ImportError:
+        for var in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
+            if os.environ.get(var, "").isdigit():
+                return int(os.environ[var])
+        return len(os.sched_getaffinity(0))
 
 
 def host_inputs(w, seqs: int):

@@ -39,8 +39,9 @@
  *     smaller tok_cap a ring (the caller keeps the window and the tail tokens of
  *     blocks not yet compressed resident).
  *   - Compressed caches are [B, n_cap, dim]; entry j of sequence b is at row j.
- *   - Every pointer must be 16-byte aligned, d and d_I multiples of 8
- *     (HA_ERR_MISALIGNED / HA_ERR_UNSUPPORTED otherwise).
+ *   - T arrays and workspaces must be 16-byte aligned; float32 / int32 arrays
+ *     4-byte aligned; d and d_I multiples of 8 (HA_ERR_MISALIGNED /
+ *     HA_ERR_UNSUPPORTED otherwise).
  *   - Arguments are checked on the host before any launch; on error nothing is
  *     launched and ha_last_error() describes the failure.  A failed launch
  *     returns HA_ERR_CUDA.  Faults of the caller's memory surface at the

@@ -79,6 +79,22 @@ bool aligned16(const void* ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15u
     HA_REQUIRE(aligned16(ptr), HA_ERR_MISALIGNED, "%s is not 16-byte aligned", #ptr); \
   } while (0)
 
+// Arrays read as scalars (positions, indices, gates, weights, scores, lse) need
+// only their natural 4-byte alignment.
+#define HA_PTR4(ptr)                                                                \
+  do {                                                                              \
+    HA_REQUIRE((ptr) != nullptr, HA_ERR_INVALID_ARG, "%s is NULL", #ptr);           \
+    HA_REQUIRE((reinterpret_cast<uintptr_t>(ptr) & 3u) == 0, HA_ERR_MISALIGNED,     \
+               "%s is not 4-byte aligned", #ptr);                                   \
+  } while (0)
+
+#define HA_OPT_PTR4(ptr)                                                              \
+  do {                                                                                \
+    if ((ptr) != nullptr)                                                             \
+      HA_REQUIRE((reinterpret_cast<uintptr_t>(ptr) & 3u) == 0, HA_ERR_MISALIGNED,     \
+                 "%s is not 4-byte aligned", #ptr);                                   \
+  } while (0)
+
 #define HA_OPT_PTR(ptr)                                                               \
   do {                                                                                \
     if ((ptr) != nullptr)                                                             \
@@ -129,8 +145,8 @@ ha_status compress_common(const ha_params* p, int n_tensors, const void* const* 
     HA_REQUIRE(aligned16(src[i]) && aligned16(dst[i]), HA_ERR_MISALIGNED,
                "tensor %d is not 16-byte aligned", i);
   }
-  HA_PTR(gate);
-  HA_PTR(blk_begin);
+  HA_PTR4(gate);
+  HA_PTR4(blk_begin);
   HA_REQUIRE(tok_cap >= p->m, HA_ERR_INVALID_ARG, "tok_cap = %d < m = %d", tok_cap, p->m);
   HA_REQUIRE(n_blk >= 0, HA_ERR_INVALID_ARG, "n_blk = %d", n_blk);
   HA_REQUIRE(n_cap >= 1, HA_ERR_INVALID_ARG, "n_cap = %d", n_cap);
@@ -196,10 +212,10 @@ ha_status csa_index_scores(const ha_params* p, const void* q_idx, const float* w
   ha_status s = check_params(p, false, true);
   if (s != HA_OK) return s;
   HA_PTR(q_idx);
-  HA_PTR(w_idx);
+  HA_PTR4(w_idx);
   HA_PTR(cki);
-  HA_PTR(q_pos);
-  HA_PTR(scores);
+  HA_PTR4(q_pos);
+  HA_PTR4(scores);
   HA_REQUIRE(n_cap >= 1, HA_ERR_INVALID_ARG, "n_cap = %d", n_cap);
   HA_REQUIRE(Tq >= 1, HA_ERR_INVALID_ARG, "Tq = %d", Tq);
   HA_REQUIRE((long long)p->B * Tq <= 0x7fffffffLL, HA_ERR_UNSUPPORTED, "B * Tq too large");
@@ -215,9 +231,9 @@ ha_status csa_topk(const ha_params* p, const float* scores, int32_t n_cap, const
   if (s != HA_OK) return s;
   s = check_k(p);
   if (s != HA_OK) return s;
-  HA_PTR(scores);
-  HA_PTR(q_pos);
-  HA_PTR(idx);
+  HA_PTR4(scores);
+  HA_PTR4(q_pos);
+  HA_PTR4(idx);
   HA_OPT_PTR(ws);
   HA_REQUIRE(n_cap >= 1, HA_ERR_INVALID_ARG, "n_cap = %d", n_cap);
   HA_REQUIRE(Tq >= 1, HA_ERR_INVALID_ARG, "Tq = %d", Tq);
@@ -245,12 +261,12 @@ ha_status hybrid_attn_decode(const ha_params* p, const void* q, const void* ck, 
   HA_PTR(q);
   HA_PTR(ck);
   HA_PTR(cv);
-  HA_OPT_PTR(idx);
+  HA_OPT_PTR4(idx);
   HA_PTR(k_tok);
   HA_PTR(v_tok);
-  HA_PTR(ctx_len);
+  HA_PTR4(ctx_len);
   HA_PTR(o);
-  HA_OPT_PTR(lse);
+  HA_OPT_PTR4(lse);
   HA_OPT_PTR(ws);
   HA_REQUIRE(n_cap >= 1, HA_ERR_INVALID_ARG, "n_cap = %d", n_cap);
   HA_REQUIRE(tok_cap >= p->n_win, HA_ERR_INVALID_ARG, "tok_cap = %d < n_win = %d", tok_cap,
@@ -276,14 +292,14 @@ ha_status hybrid_attn_prefill(const ha_params* p, const void* q, const int32_t* 
     if (s != HA_OK) return s;
   }
   HA_PTR(q);
-  HA_PTR(q_pos);
+  HA_PTR4(q_pos);
   HA_PTR(ck);
   HA_PTR(cv);
-  HA_OPT_PTR(idx);
+  HA_OPT_PTR4(idx);
   HA_PTR(k_tok);
   HA_PTR(v_tok);
   HA_PTR(o);
-  HA_OPT_PTR(lse);
+  HA_OPT_PTR4(lse);
   HA_OPT_PTR(ws);
   HA_REQUIRE(n_cap >= 1, HA_ERR_INVALID_ARG, "n_cap = %d", n_cap);
   HA_REQUIRE(Tq >= 1, HA_ERR_INVALID_ARG, "Tq = %d", Tq);

@@ -77,7 +77,8 @@ def test_index_topk_validation(lib):
     assert code_of(B.csa_index_scores, P(H_I=128, d_I=512), A, A, A, 256, A, 1, A, 0) == 3
     assert code_of(B.csa_index_scores, P(), A, A, A, 0, A, 1, A, 0) == 1
     assert code_of(B.csa_index_scores, P(), A, A, A, 256, A, 0, A, 0) == 1
-    assert code_of(B.csa_index_scores, P(), A, A + 8, A, 256, A, 1, A, 0) == 2
+    assert code_of(B.csa_index_scores, P(), A + 8, A, A, 256, A, 1, A, 0) == 2
+    assert code_of(B.csa_index_scores, P(), A, A + 2, A, 256, A, 1, A, 0) == 2
     assert code_of(B.csa_topk, P(k=0), A, 256, A, 1, A, None, 0) == 3
     assert code_of(B.csa_topk, P(k=5000), A, 256, A, 1, A, None, 0) == 3
     assert code_of(B.csa_topk, P(dtype=7), A, 256, A, 1, A, None, 0) == 1
