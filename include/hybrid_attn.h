@@ -186,6 +186,31 @@ ha_status hybrid_attn_prefill(const ha_params* p, const void* q, const int32_t* 
                               int32_t tok_cap, void* o, float* lse, void* ws, size_t ws_bytes,
                               ha_stream_t stream);
 
+/* ---------------------------------------------------------------------------
+ * hybrid_attn_decode_static -- hybrid_attn_decode without a workspace argument,
+ * for callers that cannot allocate device memory (an engine plugin that only
+ * gets its layer's input and output pointers, code living in another runtime's
+ * memory pool, serving loops that must not call cudaMalloc because it
+ * synchronises the device).  The pages have no counterpart: this is a calling
+ * convention of this library, not part of the method.
+ * Same arguments, results and checks as hybrid_attn_decode.  The split-KV
+ * partials go to a fixed 32 MiB array in device global memory owned by the
+ * library; each device that loads the library holds that array until the
+ * process exits.  Problems whose partials need more than 32 MiB
+ * (ha_workspace_size(p, HA_OP_DECODE, 1, n_cap, idx != NULL)) return
+ * HA_ERR_WORKSPACE without launching.  Allocates nothing.
+ * Every call on a device shares the array and leaves its last contents behind
+ * (no part of it needs to start at zero); calls whose kernels overlap on the GPU
+ * race on it, so order them on one stream.  The first call on a device looks up
+ * the array's device address once (with that device current); make that first
+ * call before any stream capture that records this entry point.
+ * ------------------------------------------------------------------------- */
+ha_status hybrid_attn_decode_static(const ha_params* p, const void* q, const void* ck,
+                                    const void* cv, int32_t n_cap, const int32_t* idx,
+                                    const void* k_tok, const void* v_tok, int32_t tok_cap,
+                                    const int32_t* ctx_len, void* o, float* lse,
+                                    ha_stream_t stream);
+
 /* Workspace bytes for `op` (ha_op) with Tq queries per sequence and n_cap
  * compressed entries; `is_csa` = idx will be non-NULL (decode / prefill). */
 ha_status ha_workspace_size(const ha_params* p, int32_t op, int32_t Tq, int32_t n_cap,

@@ -52,6 +52,8 @@ _SIGS = {
                            _P, _SZ, _P],
     "hybrid_attn_prefill": [ctypes.POINTER(Params), _P, _P, _I, _P, _P, _I, _P, _P, _P, _I, _P,
                             _P, _P, _SZ, _P],
+    "hybrid_attn_decode_static": [ctypes.POINTER(Params), _P, _P, _P, _I, _P, _P, _P, _I, _P, _P,
+                                  _P, _P],
     "ha_workspace_size": [ctypes.POINTER(Params), _I, _I, _I, _I, ctypes.POINTER(ctypes.c_size_t)],
 }
 EXPORTS = list(_SIGS) + ["ha_status_string", "ha_last_error", "ha_abi_version", "ha_launch_count"]
@@ -150,6 +152,18 @@ def hybrid_attn_prefill(p, q, q_pos, Tq, ck, cv, n_cap, idx, k_tok, v_tok, tok_c
     wp, wb = _ws(ws)
     _call("hybrid_attn_prefill", ctypes.byref(p), _ptr(q), _ptr(q_pos), Tq, _ptr(ck), _ptr(cv),
           n_cap, _ptr(idx), _ptr(k_tok), _ptr(v_tok), tok_cap, _ptr(o), _ptr(lse), wp, wb,
+          _stream(stream))
+
+
+STATIC_SCRATCH_BYTES = 32 << 20
+
+
+def hybrid_attn_decode_static(p, q, ck, cv, n_cap, idx, k_tok, v_tok, tok_cap, ctx_len, o,
+                              lse=None, stream=None):
+    """hybrid_attn_decode for callers that cannot allocate: no workspace argument,
+    the library's fixed 32 MiB device scratch holds the split partials."""
+    _call("hybrid_attn_decode_static", ctypes.byref(p), _ptr(q), _ptr(ck), _ptr(cv), n_cap,
+          _ptr(idx), _ptr(k_tok), _ptr(v_tok), tok_cap, _ptr(ctx_len), _ptr(o), _ptr(lse),
           _stream(stream))
 
 

@@ -159,6 +159,10 @@ ha_status compress_common(const ha_params* p, int n_tensors, const void* const* 
 
 }  // namespace
 
+void ha::set_last_error(const char* msg) {
+  snprintf(g_last_error, sizeof(g_last_error), "%s", msg);
+}
+
 extern "C" {
 
 int32_t ha_abi_version(void) { return 1; }

@@ -9,6 +9,9 @@
 
 namespace ha {
 
+// api.cu: replace the message returned by ha_last_error() on this thread.
+void set_last_error(const char* msg);
+
 // compress.cu: n_tensors row tensors compressed with the same gates.
 cudaError_t launch_compress(const ha_params& p, int n_tensors, const void* const* src,
                             void* const* dst, const int* dims, const float* gate,
