@@ -216,6 +216,12 @@ ha_status hybrid_attn_decode_static(const ha_params* p, const void* q, const voi
 ha_status ha_workspace_size(const ha_params* p, int32_t op, int32_t Tq, int32_t n_cap,
                             int32_t is_csa, size_t* bytes);
 
+/* First error code recorded on the current device by a tensor-core kernel whose
+ * pipeline wait ran out of time (0 = none); such a kernel returns early instead
+ * of hanging and its outputs are incomplete.  Blocks until the device's prior
+ * work is done.  `clear` != 0 resets the code. */
+ha_status ha_device_error(int32_t* code, int32_t clear);
+
 /* Static description of a status code. */
 const char* ha_status_string(ha_status s);
 

@@ -55,6 +55,7 @@ _SIGS = {
     "hybrid_attn_decode_static": [ctypes.POINTER(Params), _P, _P, _P, _I, _P, _P, _P, _I, _P, _P,
                                   _P, _P],
     "ha_workspace_size": [ctypes.POINTER(Params), _I, _I, _I, _I, ctypes.POINTER(ctypes.c_size_t)],
+    "ha_device_error": [ctypes.POINTER(ctypes.c_int32), _I],
 }
 EXPORTS = list(_SIGS) + ["ha_status_string", "ha_last_error", "ha_abi_version", "ha_launch_count"]
 
@@ -183,3 +184,10 @@ def ha_abi_version() -> int:
 
 def ha_launch_count() -> int:
     return load_library().ha_launch_count()
+
+
+def ha_device_error(clear: bool = True) -> int:
+    """Error code recorded by a tensor-core kernel that gave up waiting (0 = none)."""
+    code = ctypes.c_int32(0)
+    _call("ha_device_error", ctypes.byref(code), int(clear))
+    return code.value

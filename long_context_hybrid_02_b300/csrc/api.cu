@@ -223,6 +223,13 @@ ha_status csa_index_scores(const ha_params* p, const void* q_idx, const float* w
   HA_REQUIRE(n_cap >= 1, HA_ERR_INVALID_ARG, "n_cap = %d", n_cap);
   HA_REQUIRE(Tq >= 1, HA_ERR_INVALID_ARG, "Tq = %d", Tq);
   HA_REQUIRE((long long)p->B * Tq <= 0x7fffffffLL, HA_ERR_UNSUPPORTED, "B * Tq too large");
+  if (ha::index_scores_tc_supported(*p, q_idx, cki)) {
+    int* err = ha::device_error_word();
+    HA_REQUIRE(err != nullptr, HA_ERR_CUDA, "device error word unavailable");
+    return cuda_status(ha::launch_index_scores_tc(*p, q_idx, w_idx, cki, n_cap, q_pos, Tq, scores,
+                                                  err, (cudaStream_t)stream),
+                       "index launch (tensor cores)");
+  }
   return cuda_status(ha::launch_index_scores_simt(*p, q_idx, w_idx, cki, n_cap, q_pos, Tq, scores,
                                                   (cudaStream_t)stream),
                      "index launch");

@@ -1,0 +1,313 @@
+// Lightning Indexer on the tcgen05 tensor cores ("DeepSeek-V4 深度研究剖析" §5.3:
+// the indexer scores every compressed CSA entry; "EP 95 解读 DeepSeek-V4 论文": it
+// must look at everything, so it must be light).  Score formula fixed by this
+// library:  s[b,t,j] = sum_h w[b,t,h] * max(0, qI[b,t,h,:] . cI[b,j,:]).
+//
+// The scores of one query are a skinny GEMM: 64 heads x 128 dims against every
+// entry (64 flop per byte of keys), far above the CUDA-core ridge, so the heads
+// go on the tensor cores.  Entries are the M dimension (128 per tile), the QT
+// queries x 64 heads of a query group the N dimension, d_I = 128 the K dimension:
+//   D[j, (q,h)] = sum_c cI[j, c] * qI[q, h, c]      (tcgen05.mma kind::f16, fp32)
+// so that the head reduction of the epilogue stays inside one TMEM lane: each
+// epilogue thread owns one entry and sums w_h * ReLU(D) over its 64 columns per
+// query in head order.
+//
+// Persistent, warp-specialised CTA (one per SM): warp 0 streams 32 KiB key
+// tiles with TMA into a ring of kStages stages (the query group's operand is
+// loaded once per group), warp 1 issues 8 MMAs per tile into one of two TMEM
+// accumulators, warps 2-5 drain the accumulators and write the scores.  The
+// work list is every (sequence, query group, 128-entry tile) with at least one
+// eligible entry, split evenly across CTAs in (group, tile) order.  Decode uses
+// QT = 1 (N = 64), prefill QT = 4 (N = 256).
+#include "common.cuh"
+#include "kernels.h"
+#include "tc.cuh"
+#include "tc_host.h"
+
+namespace ha {
+namespace {
+
+constexpr int kHeads = 64;      // H_I handled by this kernel
+constexpr int kDim = 128;       // d_I handled by this kernel
+constexpr int kTileM = 128;     // entries per tile
+constexpr int kThreads = 192;   // 6 warps
+constexpr int kTileBytes = kTileM * kDim * 2;   // 32 KiB
+
+template <int QT> struct Cfg {
+  static constexpr int N = QT * kHeads;
+  static constexpr int kStages = QT == 1 ? 6 : (QT == 2 ? 5 : 4);
+  static constexpr int kQBytes = N * kDim * 2;
+  static constexpr int kTmemCols = 2 * N < 32 ? 32 : 2 * N;
+  static constexpr size_t kSmem = 1024 + size_t(kStages) * kTileBytes + kQBytes +
+                                  4 * QT * kHeads * sizeof(float) + 256;
+};
+
+struct IdxArgs {
+  const float* w;          // [B*Tq, H_I]
+  const int32_t* q_pos;    // [B*Tq]
+  float* scores;           // [B*Tq, n_cap]
+  int B, Tq, n_cap, n_win, m, elig;
+  int* err;
+};
+
+// Tiles of group g = (b, qg): ceil(max n_elig over its queries / 128).
+template <int QT>
+__device__ __forceinline__ int group_tiles(const IdxArgs& a, int g) {
+  const int gpb = (a.Tq + QT - 1) / QT;
+  const int b = g / gpb, q0 = (g % gpb) * QT;
+  int ne = 0;
+#pragma unroll
+  for (int q = 0; q < QT; ++q)
+    if (q0 + q < a.Tq) ne = max(ne, n_eligible(a.q_pos[b * a.Tq + q0 + q], a.n_win, a.m, a.elig, a.n_cap));
+  return (ne + kTileM - 1) / kTileM;
+}
+
+// Walk over this CTA's tiles in (group, tile) order.  Every role warp runs the
+// same walk; init() scans all groups with the whole warp.
+template <int QT>
+struct TileWalk {
+  int g, t, tiles_g, left, n_groups;
+  __device__ bool init(const IdxArgs& a) {
+    const int lane = threadIdx.x & 31;
+    n_groups = a.B * ((a.Tq + QT - 1) / QT);
+    long long total = 0;
+    for (int base = 0; base < n_groups; base += 32) {
+      const int gg = base + lane;
+      int c = gg < n_groups ? group_tiles<QT>(a, gg) : 0;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) c += __shfl_xor_sync(0xffffffffu, c, o);
+      total += c;
+    }
+    const long long lo = total * blockIdx.x / gridDim.x;
+    const long long hi = total * (blockIdx.x + 1) / gridDim.x;
+    left = int(hi - lo);
+    if (left <= 0) return false;
+    // find the group holding tile `lo`
+    long long run = 0;
+    g = 0;
+    for (int base = 0; base < n_groups; base += 32) {
+      const int gg = base + lane;
+      const int c = gg < n_groups ? group_tiles<QT>(a, gg) : 0;
+      int incl = c;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+      }
+      const int tot = __shfl_sync(0xffffffffu, incl, 31);
+      if (run + tot > lo) {
+        const unsigned hit = __ballot_sync(0xffffffffu, run + incl > lo);
+        const int l = __ffs(hit) - 1;
+        const int excl = __shfl_sync(0xffffffffu, incl - c, l);
+        g = base + l;
+        t = int(lo - run - excl);
+        tiles_g = __shfl_sync(0xffffffffu, c, l);
+        return true;
+      }
+      run += tot;
+    }
+    return false;
+  }
+  // Advance to the next tile; returns false at the end of the range.
+  __device__ bool next(const IdxArgs& a) {
+    if (--left <= 0) return false;
+    if (++t >= tiles_g) {
+      do {
+        ++g;
+        tiles_g = g < n_groups ? group_tiles<QT>(a, g) : 1;
+      } while (tiles_g == 0);
+      t = 0;
+    }
+    return true;
+  }
+  __device__ bool last_of_group() const { return left == 1 || t + 1 >= tiles_g; }
+};
+
+template <int QT>
+__global__ void __launch_bounds__(kThreads, 1)
+    index_scores_tc(const __grid_constant__ CUtensorMap map_k,
+                    const __grid_constant__ CUtensorMap map_q, IdxArgs a) {
+  using C = Cfg<QT>;
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char* base = reinterpret_cast<unsigned char*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  unsigned char* s_k = base;                                   // kStages x 32 KiB
+  unsigned char* s_q = s_k + size_t(C::kStages) * kTileBytes;  // QT x 16 KiB
+  float* s_w = reinterpret_cast<float*>(s_q + C::kQBytes);     // [4 warps][QT][64]
+  uint64_t* bars = reinterpret_cast<uint64_t*>(s_w + 4 * QT * kHeads);
+  uint64_t* full = bars;                   // [kStages]
+  uint64_t* empty = full + C::kStages;     // [kStages]
+  uint64_t* acc_full = empty + C::kStages; // [2]
+  uint64_t* acc_empty = acc_full + 2;      // [2]
+  uint64_t* q_full = acc_empty + 2;
+  uint64_t* q_empty = q_full + 1;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(q_empty + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  TileWalk<QT> walk;
+  const bool have = walk.init(a);      // identical in every warp
+  if (!have) return;                   // CTA-uniform
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::kStages; ++s) { tc::mbar_init(&full[s], 1); tc::mbar_init(&empty[s], 1); }
+    for (int i = 0; i < 2; ++i) { tc::mbar_init(&acc_full[i], 1); tc::mbar_init(&acc_empty[i], 4); }
+    tc::mbar_init(q_full, 1);
+    tc::mbar_init(q_empty, 1);
+    tc::fence_mbar_init();
+  }
+  if (warp == 1) { tc::tmem_alloc(tmem_slot, C::kTmemCols); tc::tmem_relinquish(); }
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tmem = *tmem_slot;
+  const int gpb = (a.Tq + QT - 1) / QT;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      tc::tma_prefetch(&map_k);
+      tc::tma_prefetch(&map_q);
+      int i = 0, prev_g = -1, n_groups_seen = 0;
+      do {
+        if (walk.g != prev_g) {
+          if (prev_g >= 0 && !tc::mbar_wait(q_empty, (n_groups_seen - 1) & 1, a.err, 11)) break;
+          const int b = walk.g / gpb, q0 = (walk.g % gpb) * QT;
+          const int y = (b * a.Tq + q0) * kHeads;
+          tc::mbar_expect_tx(q_full, C::kQBytes);
+          tc::tma_load_2d(s_q, &map_q, 0, y, q_full);
+          tc::tma_load_2d(s_q + C::kQBytes / 2, &map_q, 64, y, q_full);
+          prev_g = walk.g;
+          ++n_groups_seen;
+        }
+        const int s = i % C::kStages;
+        if (!tc::mbar_wait(&empty[s], ((i / C::kStages) & 1) ^ 1, a.err, 12)) break;
+        const int b = walk.g / gpb;
+        const int y = b * a.n_cap + walk.t * kTileM;
+        unsigned char* dst = s_k + size_t(s) * kTileBytes;
+        tc::mbar_expect_tx(&full[s], kTileBytes);
+        tc::tma_load_2d(dst, &map_k, 0, y, &full[s]);
+        tc::tma_load_2d(dst + kTileBytes / 2, &map_k, 64, y, &full[s]);
+        ++i;
+      } while (walk.next(a));
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc = tc::idesc_bf16_f32(kTileM, C::N);
+      const uint32_t k_base = tc::smem_u32(s_k), q_base = tc::smem_u32(s_q);
+      int i = 0, prev_g = -1, n_groups_seen = 0;
+      do {
+        if (walk.g != prev_g) {
+          if (!tc::mbar_wait(q_full, n_groups_seen & 1, a.err, 21)) break;
+          prev_g = walk.g;
+          ++n_groups_seen;
+        }
+        const int s = i % C::kStages, acc = i & 1;
+        if (!tc::mbar_wait(&full[s], (i / C::kStages) & 1, a.err, 22)) break;
+        if (!tc::mbar_wait(&acc_empty[acc], ((i >> 1) & 1) ^ 1, a.err, 23)) break;
+        tc::fence_after_sync();
+        const uint32_t kb = k_base + s * kTileBytes;
+#pragma unroll
+        for (int kk = 0; kk < kDim / 16; ++kk) {
+          const uint32_t off_k = (kk >> 2) * (kTileBytes / 2) + (kk & 3) * 32;
+          const uint32_t off_q = (kk >> 2) * (C::kQBytes / 2) + (kk & 3) * 32;
+          tc::mma_bf16(tmem + acc * C::N, tc::sdesc_kmajor_sw128(kb + off_k),
+                       tc::sdesc_kmajor_sw128(q_base + off_q), idesc, kk > 0 ? 1u : 0u);
+        }
+        tc::mma_commit(&empty[s]);
+        tc::mma_commit(&acc_full[acc]);
+        if (walk.last_of_group()) tc::mma_commit(q_empty);
+        ++i;
+      } while (walk.next(a));
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue (warps 2..5)
+    const int quarter = warp & 3;                     // TMEM lanes 32*quarter ..
+    const int row = quarter * 32 + lane;              // entry within the tile
+    float* w_mine = s_w + (warp - 2) * QT * kHeads;   // this warp's copy of the weights
+    int i = 0, prev_g = -1;
+    bool ok = true;
+    do {
+      const int b = walk.g / gpb, q0 = (walk.g % gpb) * QT;
+      if (walk.g != prev_g) {                         // warp-private: no cross-warp barrier
+        __syncwarp();
+        for (int x = lane; x < QT * kHeads; x += 32) {
+          const int q = x / kHeads;
+          w_mine[x] = (q0 + q < a.Tq) ? a.w[(long long)(b * a.Tq + q0 + q) * kHeads + x % kHeads] : 0.f;
+        }
+        __syncwarp();
+        prev_g = walk.g;
+      }
+      const int acc = i & 1;
+      ok = tc::mbar_wait(&acc_full[acc], (i >> 1) & 1, a.err, 31);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+      tc::fence_after_sync();
+      const int j = walk.t * kTileM + row;
+#pragma unroll 1
+      for (int q = 0; q < QT; ++q) {
+        float s = 0.f;
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+          float v[32];
+          tc::tmem_ld32(tmem + (uint32_t(quarter * 32) << 16) + acc * C::N + q * kHeads + half * 32, v);
+#pragma unroll
+          for (int h = 0; h < 32; ++h) s = fmaf(w_mine[q * kHeads + half * 32 + h], fmaxf(v[h], 0.f), s);
+        }
+        if (q0 + q < a.Tq) {
+          const long long r = (long long)b * a.Tq + q0 + q;
+          const int ne = n_eligible(a.q_pos[r], a.n_win, a.m, a.elig, a.n_cap);
+          if (j < ne) a.scores[r * a.n_cap + j] = s;
+        }
+      }
+      tc::fence_before_sync();
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(&acc_empty[acc]);
+      ++i;
+    } while (walk.next(a));
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  if (warp == 1) tc::tmem_dealloc(tmem, C::kTmemCols);
+}
+
+int g_num_sms = 0;
+
+template <int QT>
+cudaError_t launch_qt(const ha_params& p, const void* q_idx, const float* w_idx, const void* cki,
+                      int n_cap, const int32_t* q_pos, int Tq, float* scores, int* err,
+                      cudaStream_t st) {
+  using C = Cfg<QT>;
+  CUtensorMap map_k, map_q;
+  cudaError_t e = make_tmap_bf16_2d(&map_k, cki, kDim, uint64_t(p.B) * n_cap, kDim * 2, 64, kTileM);
+  if (e != cudaSuccess) return e;
+  e = make_tmap_bf16_2d(&map_q, q_idx, kDim, uint64_t(p.B) * Tq * kHeads, kDim * 2, 64, C::N);
+  if (e != cudaSuccess) return e;
+  e = ensure_smem(reinterpret_cast<const void*>(index_scores_tc<QT>), C::kSmem);
+  if (e != cudaSuccess) return e;
+  if (g_num_sms == 0) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    e = cudaDeviceGetAttribute(&g_num_sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+  }
+  IdxArgs a{w_idx, q_pos, scores, p.B, Tq, n_cap, p.n_win, p.m, p.elig, err};
+  index_scores_tc<QT><<<g_num_sms, kThreads, C::kSmem, st>>>(map_k, map_q, a);
+  return launched(cudaGetLastError());
+}
+
+}  // namespace
+
+bool index_scores_tc_supported(const ha_params& p, const void* q_idx, const void* cki) {
+  return p.dtype == HA_BF16 && p.H_I == kHeads && p.d_I == kDim &&
+         (reinterpret_cast<uintptr_t>(q_idx) & 15) == 0 && (reinterpret_cast<uintptr_t>(cki) & 15) == 0;
+}
+
+cudaError_t launch_index_scores_tc(const ha_params& p, const void* q_idx, const float* w_idx,
+                                   const void* cki, int n_cap, const int32_t* q_pos, int Tq,
+                                   float* scores, int* err, cudaStream_t st) {
+  if (Tq >= 4) return launch_qt<4>(p, q_idx, w_idx, cki, n_cap, q_pos, Tq, scores, err, st);
+  return launch_qt<1>(p, q_idx, w_idx, cki, n_cap, q_pos, Tq, scores, err, st);
+}
+
+}  // namespace ha

@@ -12,6 +12,10 @@ namespace ha {
 // api.cu: replace the message returned by ha_last_error() on this thread.
 void set_last_error(const char* msg);
 
+// status.cu: device address of the error word of the tensor-core kernels on the
+// current device (null if it cannot be looked up).
+int* device_error_word();
+
 // compress.cu: n_tensors row tensors compressed with the same gates.
 cudaError_t launch_compress(const ha_params& p, int n_tensors, const void* const* src,
                             void* const* dst, const int* dims, const float* gate,
@@ -22,6 +26,12 @@ cudaError_t launch_compress(const ha_params& p, int n_tensors, const void* const
 cudaError_t launch_index_scores_simt(const ha_params& p, const void* q_idx, const float* w_idx,
                                      const void* cki, int n_cap, const int32_t* q_pos, int Tq,
                                      float* scores, cudaStream_t st);
+
+// indexer_tc.cu: tcgen05 indexer for bf16, H_I = 64, d_I = 128.
+bool index_scores_tc_supported(const ha_params& p, const void* q_idx, const void* cki);
+cudaError_t launch_index_scores_tc(const ha_params& p, const void* q_idx, const float* w_idx,
+                                   const void* cki, int n_cap, const int32_t* q_pos, int Tq,
+                                   float* scores, int* err, cudaStream_t st);
 
 // topk.cu
 size_t topk_workspace_bytes(const ha_params& p, int Tq, int n_cap);
