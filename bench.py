@@ -44,6 +44,9 @@ def parse():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--batch", type=int, default=0,
+                    help="sequences (default: the workload's own batch); a smaller batch is a "
+                         "smaller workload for profiler captures, not a bench line")
     return ap.parse_args()
 
 
@@ -267,6 +270,8 @@ def main():
         bld.build()
     B.load_library()
     w = synth.WORKLOADS[args.workload]
+    if args.batch > 0:
+        w = w.scaled(B=args.batch)
     assert w.decode, "the benchmark times decode workloads"
     tok = synth.make_tokens(w, dev)
     qry = synth.make_queries(w, dev)

@@ -134,6 +134,16 @@ int max_keys(const ha_params* p, int n_cap, bool is_csa) {
   return (is_csa ? p->k : n_cap) + p->n_win;
 }
 
+// Launch plan of the attention calls: the tensor-core kernel where it applies (its
+// workspace does not depend on tok_cap, so ha_workspace_size passes 0 for it),
+// else the CUDA-core kernel.
+ha::AttnPlan attention_plan(const ha_params* p, int rows, int n_cap, int tok_cap, bool is_csa,
+                            bool decode) {
+  if (ha::attention_tc_supported(*p, n_cap, tok_cap))
+    return ha::plan_attention_tc(*p, rows, max_keys(p, n_cap, is_csa));
+  return ha::plan_attention_simt(*p, rows, max_keys(p, n_cap, is_csa), decode);
+}
+
 ha_status compress_common(const ha_params* p, int n_tensors, const void* const* src,
                           void* const* dst, const int* dims, const float* gate, int32_t tok_cap,
                           const int32_t* blk_begin, int32_t n_blk, int32_t n_cap,
@@ -282,9 +292,18 @@ ha_status hybrid_attn_decode(const ha_params* p, const void* q, const void* ck, 
   HA_REQUIRE(n_cap >= 1, HA_ERR_INVALID_ARG, "n_cap = %d", n_cap);
   HA_REQUIRE(tok_cap >= p->n_win, HA_ERR_INVALID_ARG, "tok_cap = %d < n_win = %d", tok_cap,
              p->n_win);
-  const ha::AttnPlan pl = ha::plan_attention_simt(*p, p->B, max_keys(p, n_cap, idx != nullptr), true);
+  const bool tc = ha::attention_tc_supported(*p, n_cap, tok_cap);
+  const ha::AttnPlan pl = attention_plan(p, p->B, n_cap, tok_cap, idx != nullptr, true);
   HA_REQUIRE(ws_bytes >= pl.ws_bytes && (pl.ws_bytes == 0 || ws != nullptr), HA_ERR_WORKSPACE,
              "workspace %zu bytes < %zu", ws_bytes, pl.ws_bytes);
+  if (tc) {
+    int* err = ha::device_error_word();
+    HA_REQUIRE(err != nullptr, HA_ERR_CUDA, "device error word unavailable");
+    return cuda_status(ha::launch_attention_tc(*p, pl, 1, 1, q, ctx_len, ck, cv, n_cap, idx, k_tok,
+                                               v_tok, tok_cap, o, lse, ws, err,
+                                               (cudaStream_t)stream),
+                       "decode launch (tensor cores)");
+  }
   return cuda_status(ha::launch_attention_simt(*p, pl, 1, 1, q, ctx_len, ck, cv, n_cap, idx, k_tok,
                                                v_tok, tok_cap, o, lse, ws, (cudaStream_t)stream),
                      "decode launch");
@@ -317,10 +336,18 @@ ha_status hybrid_attn_prefill(const ha_params* p, const void* q, const int32_t* 
   HA_REQUIRE((long long)p->B * Tq <= 0x7fffffffLL, HA_ERR_UNSUPPORTED, "B * Tq too large");
   HA_REQUIRE(tok_cap >= p->n_win, HA_ERR_INVALID_ARG, "tok_cap = %d < n_win = %d", tok_cap,
              p->n_win);
-  const ha::AttnPlan pl =
-      ha::plan_attention_simt(*p, p->B * Tq, max_keys(p, n_cap, idx != nullptr), false);
+  const bool tc = ha::attention_tc_supported(*p, n_cap, tok_cap);
+  const ha::AttnPlan pl = attention_plan(p, p->B * Tq, n_cap, tok_cap, idx != nullptr, false);
   HA_REQUIRE(ws_bytes >= pl.ws_bytes && (pl.ws_bytes == 0 || ws != nullptr), HA_ERR_WORKSPACE,
              "workspace %zu bytes < %zu", ws_bytes, pl.ws_bytes);
+  if (tc) {
+    int* err = ha::device_error_word();
+    HA_REQUIRE(err != nullptr, HA_ERR_CUDA, "device error word unavailable");
+    return cuda_status(ha::launch_attention_tc(*p, pl, 0, Tq, q, q_pos, ck, cv, n_cap, idx, k_tok,
+                                               v_tok, tok_cap, o, lse, ws, err,
+                                               (cudaStream_t)stream),
+                       "prefill launch (tensor cores)");
+  }
   return cuda_status(ha::launch_attention_simt(*p, pl, 0, Tq, q, q_pos, ck, cv, n_cap, idx, k_tok,
                                                v_tok, tok_cap, o, lse, ws, (cudaStream_t)stream),
                      "prefill launch");
@@ -337,10 +364,10 @@ ha_status ha_workspace_size(const ha_params* p, int32_t op, int32_t Tq, int32_t 
   switch (op) {
     case HA_OP_TOPK: *bytes = ha::topk_workspace_bytes(*p, Tq, n_cap); return HA_OK;
     case HA_OP_DECODE:
-      *bytes = ha::plan_attention_simt(*p, p->B, max_keys(p, n_cap, is_csa != 0), true).ws_bytes;
+      *bytes = attention_plan(p, p->B, n_cap, 0, is_csa != 0, true).ws_bytes;
       return HA_OK;
     case HA_OP_PREFILL:
-      *bytes = ha::plan_attention_simt(*p, p->B * Tq, max_keys(p, n_cap, is_csa != 0), false).ws_bytes;
+      *bytes = attention_plan(p, p->B * Tq, n_cap, 0, is_csa != 0, false).ws_bytes;
       return HA_OK;
   }
   return fail(HA_ERR_INVALID_ARG, "op = %d", op);

@@ -238,6 +238,17 @@ cudaError_t launch_t(const AttnArgs& a, int rows, cudaStream_t st) {
 
 }  // namespace
 
+cudaError_t launch_attn_merge(const ha_params& p, int rows, int S, const float* o_part,
+                              const float* lse_part, void* o, float* lse, cudaStream_t st) {
+  if (p.dtype == HA_BF16)
+    attn_merge<__nv_bfloat16><<<dim3(rows, p.H), 128, 0, st>>>(
+        o_part, lse_part, S, p.H, p.d, static_cast<__nv_bfloat16*>(o), lse);
+  else
+    attn_merge<float><<<dim3(rows, p.H), 128, 0, st>>>(o_part, lse_part, S, p.H, p.d,
+                                                       static_cast<float*>(o), lse);
+  return launched(cudaGetLastError());
+}
+
 AttnPlan plan_attention_simt(const ha_params& p, int rows, int max_keys, bool decode) {
   AttnPlan pl{};
   const int elt = p.dtype == HA_BF16 ? 2 : 4;

@@ -51,5 +51,18 @@ cudaError_t launch_attention_simt(const ha_params& p, const AttnPlan& pl, int de
                                   const void* cv, int n_cap, const int32_t* idx,
                                   const void* k_tok, const void* v_tok, int tok_cap, void* o,
                                   float* lse, void* ws, cudaStream_t st);
+// o = merge of the S float32 partials [rows, S, H, d] + lse [rows, S, H], in split order.
+cudaError_t launch_attn_merge(const ha_params& p, int rows, int S, const float* o_part,
+                              const float* lse_part, void* o, float* lse, cudaStream_t st);
+
+// attention_tc.cu: tcgen05 attention for bf16, d = 512, H a multiple of 64 (decode
+// rows and prefill rows alike; each row has its own key list).
+bool attention_tc_supported(const ha_params& p, int n_cap, int tok_cap);
+AttnPlan plan_attention_tc(const ha_params& p, int rows, int max_keys);
+cudaError_t launch_attention_tc(const ha_params& p, const AttnPlan& pl, int decode, int Tq,
+                                const void* q, const int32_t* pos, const void* ck, const void* cv,
+                                int n_cap, const int32_t* idx, const void* k_tok,
+                                const void* v_tok, int tok_cap, void* o, float* lse, void* ws,
+                                int* err, cudaStream_t st);
 
 }  // namespace ha

@@ -92,6 +92,33 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, i
       : "memory");
 }
 
+// ---------------------------------------------------------------- cp.async (16 bytes)
+// Copy 16 bytes global -> shared through L2 only (no L1 allocation).
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+// Wait until at most N of this thread's committed groups are still in flight.
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+// Order this thread's completed generic-proxy shared-memory writes (st.shared,
+// cp.async) before later async-proxy reads (tcgen05.mma operands).
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+// Warm L2 with `bytes` (multiple of 16) starting at a 16-byte aligned address.
+__device__ __forceinline__ void prefetch_l2(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+// Barrier over `count` threads (a multiple of 32) of the CTA with id `id` (1..15).
+__device__ __forceinline__ void named_barrier(int id, int count) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
 // ---------------------------------------------------------------- tensor memory
 // Allocation by one full warp; the TMEM address is written to *slot.
 __device__ __forceinline__ void tmem_alloc(uint32_t* slot, uint32_t ncols) {
@@ -126,12 +153,29 @@ __device__ __forceinline__ uint64_t sdesc_kmajor_sw128(uint32_t saddr) {
   d |= uint64_t(2) << 61;                          // 128-byte swizzle
   return d;
 }
-// Instruction descriptor of kind::f16 with bf16 A/B, fp32 accumulate, both
-// operands K-major, shape M x N.
-__host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
+// Shared-memory matrix descriptor of a 128-byte-swizzled operand with explicit
+// leading / stride byte offsets.  For an MN-major operand (the M or N dim
+// contiguous) the canonical layout is: 64 MN elements (128 bytes) per K-row, 8
+// K-rows 128 bytes apart form a 1024-byte atom, consecutive 64-element MN chunks
+// are `lbo` bytes apart and consecutive 8-row K groups `sbo` bytes apart.
+__device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  uint64_t d = 0;
+  d |= uint64_t((saddr & 0x3FFFFu) >> 4);
+  d |= uint64_t((lbo >> 4) & 0x3FFFu) << 16;
+  d |= uint64_t((sbo >> 4) & 0x3FFFu) << 32;
+  d |= uint64_t(1) << 46;
+  d |= uint64_t(2) << 61;
+  return d;
+}
+// Instruction descriptor of kind::f16 with bf16 A/B, fp32 accumulate, shape
+// M x N; a_mn / b_mn select the MN-major (transposed) form of A / B.
+__host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool a_mn = false,
+                                                      bool b_mn = false) {
   return (1u << 4)                          // D format fp32
          | (1u << 7)                        // A format bf16
          | (1u << 10)                       // B format bf16
+         | (uint32_t(a_mn ? 1 : 0) << 15)   // A major-ness
+         | (uint32_t(b_mn ? 1 : 0) << 16)   // B major-ness
          | (uint32_t(N >> 3) << 17)         // N / 8
          | (uint32_t(M >> 4) << 24);        // M / 16
 }
