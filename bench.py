@@ -27,7 +27,6 @@ import math
 import os
 import re
 import statistics
-import subprocess
 import sys
 import time
 
@@ -44,6 +43,9 @@ def parse():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--ctx", type=int, default=0,
+                    help="context length (default: the workload's own); a shorter context is a "
+                         "smaller workload for profiler captures, not a bench line")
     ap.add_argument("--batch", type=int, default=0,
                     help="sequences (default: the workload's own batch); a smaller batch is a "
                          "smaller workload for profiler captures, not a bench line")
@@ -52,58 +54,90 @@ def parse():
 
 # ----------------------------------------------------------------------------- clocks
 class ClockSampler:
-    """nvidia-smi sampling of SM clock and throttle reasons during the timed region."""
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
-              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    """SM clock and clock-event (throttle) reasons sampled during the timed region.
 
-    def __init__(self, gpu_index: int):
-        self.gpu = gpu_index
-        self.proc = None
-        self.path = os.path.join("/tmp", f"ha_clocks_{os.getpid()}.csv")
+    Polls the driver's NVML library (read-only queries, through ctypes) from a
+    background thread every ~2 ms; the device is found by its PCI bus id, so
+    CUDA_VISIBLE_DEVICES remapping does not matter.
+    """
+    REASONS = {"hw_slowdown": 0x8, "hw_thermal_slowdown": 0x40, "sw_thermal_slowdown": 0x20,
+               "sw_power_cap": 0x4, "hw_power_brake_slowdown": 0x80}
+
+    def __init__(self, torch_device):
+        self.dev = torch_device
+        self.sm, self.reasons, self.smax = [], set(), None
+        self.err = None
+        self.thread = None
+
+    def _open_nvml(self):
+        """The driver's NVML through ctypes: (query functions, device handle)."""
+        import ctypes
+        import torch
+        lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if lib.nvmlInit_v2() != 0:
+            raise RuntimeError("nvmlInit failed")
+        pr = torch.cuda.get_device_properties(self.dev)
+        bus = f"{pr.pci_domain_id:08x}:{pr.pci_bus_id:02x}:{pr.pci_device_id:02x}.0".encode()
+        h = ctypes.c_void_p()
+        if lib.nvmlDeviceGetHandleByPciBusId_v2(bus, ctypes.byref(h)) != 0:
+            raise RuntimeError("device not found by PCI bus id")
+        reasons_fn = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            lib.nvmlDeviceGetCurrentClocksThrottleReasons
+        NVML_CLOCK_SM = 1
+
+        def clock(fn):
+            v = ctypes.c_uint()
+            if fn(h, NVML_CLOCK_SM, ctypes.byref(v)) != 0:
+                raise RuntimeError("clock query failed")
+            return int(v.value)
+
+        def reasons():
+            v = ctypes.c_ulonglong()
+            if reasons_fn(h, ctypes.byref(v)) != 0:
+                raise RuntimeError("reason query failed")
+            return int(v.value)
+
+        return (lambda: clock(lib.nvmlDeviceGetClockInfo),
+                lambda: clock(lib.nvmlDeviceGetMaxClockInfo), reasons)
 
     def __enter__(self):
+        import threading
         try:
-            self.fh = open(self.path, "w")
-            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
-                                          "--format=csv,noheader,nounits", "-lms", "200"],
-                                         stdout=self.fh, stderr=subprocess.DEVNULL)
-        except OSError:
-            self.proc = None
-        time.sleep(0.3)
+            sm_clock, max_clock, reasons = self._open_nvml()
+            self.smax = max_clock()
+        except Exception as e:          # NVML missing: report it, do not guess
+            self.err = f"nvml unavailable: {type(e).__name__}: {e}"
+            return self
+        self.stop = threading.Event()
+
+        def poll():
+            while not self.stop.is_set():
+                try:
+                    self.sm.append(sm_clock())
+                    bits = reasons()
+                    for name, bit in self.REASONS.items():
+                        if bits & bit:
+                            self.reasons.add(name)
+                except Exception as e:
+                    self.err = f"nvml query failed: {e}"
+                    return
+                time.sleep(0.002)
+
+        self.thread = threading.Thread(target=poll, daemon=True)
+        self.thread.start()
+        time.sleep(0.01)
         return self
 
     def __exit__(self, *exc):
-        if self.proc is not None:
-            self.proc.terminate()
-            try:
-                self.proc.wait(timeout=5)
-            except subprocess.TimeoutExpired:
-                self.proc.kill()
-            self.fh.close()
+        if self.thread is not None:
+            self.stop.set()
+            self.thread.join(timeout=5)
 
     def summary(self):
-        if self.proc is None or not os.path.exists(self.path):
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
-        sm, smax, reasons = [], [], set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for line in open(self.path):
-            parts = [x.strip() for x in line.split(",")]
-            if len(parts) < 9:
-                continue
-            try:
-                sm.append(float(parts[1]))
-                smax.append(float(parts[2]))
-            except ValueError:
-                continue
-            for n, v in zip(names, parts[5:9]):
-                if v.lower() == "active":
-                    reasons.add(n)
-        os.unlink(self.path)
-        if not sm:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
-                "samples": len(sm)}
+        if not self.sm:
+            return {"sm_mhz": None, "sm_max_mhz": self.smax, "reasons": [self.err or "no samples"]}
+        return {"sm_mhz": statistics.median(self.sm), "sm_max_mhz": self.smax,
+                "reasons": sorted(self.reasons), "samples": len(self.sm), "source": "nvml"}
 
 
 # ----------------------------------------------------------------------------- helpers
@@ -272,6 +306,8 @@ def main():
     w = synth.WORKLOADS[args.workload]
     if args.batch > 0:
         w = w.scaled(B=args.batch)
+    if args.ctx > 0:
+        w = w.scaled(L=args.ctx)
     assert w.decode, "the benchmark times decode workloads"
     tok = synth.make_tokens(w, dev)
     qry = synth.make_queries(w, dev)
@@ -334,7 +370,7 @@ def main():
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
-    with ClockSampler(local) as clocks:
+    with ClockSampler(dev) as clocks:
         t_wall0 = time.perf_counter()
         tot, per = timed(args.steps)
         torch.cuda.synchronize()

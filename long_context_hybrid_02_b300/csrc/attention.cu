@@ -175,29 +175,68 @@ __global__ void __launch_bounds__(kThreads) attn_simt(AttnArgs a) {
 }
 
 // o = sum_s exp(lse_s - LSE) o_s, LSE = log sum_s exp(lse_s), splits in order.
+// One CTA per (row, head): the split weights once into shared memory, then 4-dim
+// groups with up to 8 splits' loads in flight before they are combined.
+__device__ __forceinline__ void store4(float* o, const float4& v) {
+  *reinterpret_cast<float4*>(o) = v;
+}
+__device__ __forceinline__ void store4(__nv_bfloat16* o, const float4& v) {
+  const __nv_bfloat162 lo = __floats2bfloat162_rn(v.x, v.y), hi = __floats2bfloat162_rn(v.z, v.w);
+  uint2 pk;
+  pk.x = *reinterpret_cast<const uint32_t*>(&lo);
+  pk.y = *reinterpret_cast<const uint32_t*>(&hi);
+  *reinterpret_cast<uint2*>(o) = pk;
+}
+
 template <typename T>
 __global__ void __launch_bounds__(128) attn_merge(const float* __restrict__ o_part,
                                                   const float* __restrict__ lse_part, int S,
                                                   int H, int d, T* __restrict__ o,
                                                   float* __restrict__ lse) {
+  extern __shared__ float wts[];                  // [S]
+  __shared__ float s_inv;
   const int row = blockIdx.x, h = blockIdx.y;
   const float* lp = lse_part + (long long)row * S * H + h;
-  float mx = -INFINITY;
-  for (int s = 0; s < S; ++s) mx = fmaxf(mx, lp[(long long)s * H]);
-  float tot = 0.f;
-  if (mx != -INFINITY)
-    for (int s = 0; s < S; ++s) tot += expf(lp[(long long)s * H] - mx);
-  const float inv = tot > 0.f ? 1.f / tot : 0.f;
-  for (int c = threadIdx.x; c < d; c += blockDim.x) {
-    float acc = 0.f;
-    if (mx != -INFINITY)
-      for (int s = 0; s < S; ++s) {
-        const float wgt = expf(lp[(long long)s * H] - mx);
-        acc = fmaf(wgt, o_part[(((long long)row * S + s) * H + h) * d + c], acc);
-      }
-    o[((long long)row * H + h) * d + c] = from_f32<T>(acc * inv);
+  if (threadIdx.x < 32) {
+    float mx = -INFINITY;
+    for (int s = threadIdx.x; s < S; s += 32) mx = fmaxf(mx, lp[(long long)s * H]);
+    mx = warp_max(mx);
+    float tot = 0.f;
+    for (int s = threadIdx.x; s < S; s += 32) {
+      const float w = mx == -INFINITY ? 0.f : expf(lp[(long long)s * H] - mx);
+      wts[s] = w;
+      tot += w;
+    }
+    tot = warp_sum(tot);
+    if (threadIdx.x == 0) {
+      s_inv = tot > 0.f ? 1.f / tot : 0.f;
+      if (lse) lse[(long long)row * H + h] = tot > 0.f ? mx + logf(tot) : -INFINITY;
+    }
   }
-  if (lse && threadIdx.x == 0) lse[(long long)row * H + h] = tot > 0.f ? mx + logf(tot) : -INFINITY;
+  __syncthreads();
+  const float inv = s_inv;
+  const float* base = o_part + ((long long)row * S * H + h) * d;
+  const long long sstride = (long long)H * d;
+  for (int c = 4 * threadIdx.x; c < d; c += 4 * blockDim.x) {
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int s0 = 0; s0 < S; s0 += 8) {
+      float4 v[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        if (s0 + j < S) v[j] = __ldcg(reinterpret_cast<const float4*>(base + (s0 + j) * sstride + c));
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        if (s0 + j < S) {
+          const float w = wts[s0 + j];
+          acc.x = fmaf(w, v[j].x, acc.x);
+          acc.y = fmaf(w, v[j].y, acc.y);
+          acc.z = fmaf(w, v[j].z, acc.z);
+          acc.w = fmaf(w, v[j].w, acc.w);
+        }
+    }
+    store4(o + ((long long)row * H + h) * d + c,
+           make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv));
+  }
 }
 
 int dpl_for(int d) {
@@ -231,8 +270,8 @@ cudaError_t launch_t(const AttnArgs& a, int rows, cudaStream_t st) {
     default: e = launch_dpl<T, 32>(a, rows, smem, st); break;
   }
   if (e != cudaSuccess || a.n_splits == 1) return e;
-  attn_merge<T><<<dim3(rows, a.H), 128, 0, st>>>(a.o_part, a.lse_part, a.n_splits, a.H, a.d,
-                                                 static_cast<T*>(a.o), a.lse);
+  attn_merge<T><<<dim3(rows, a.H), 128, a.n_splits * sizeof(float), st>>>(
+      a.o_part, a.lse_part, a.n_splits, a.H, a.d, static_cast<T*>(a.o), a.lse);
   return launched(cudaGetLastError());
 }
 
@@ -241,11 +280,11 @@ cudaError_t launch_t(const AttnArgs& a, int rows, cudaStream_t st) {
 cudaError_t launch_attn_merge(const ha_params& p, int rows, int S, const float* o_part,
                               const float* lse_part, void* o, float* lse, cudaStream_t st) {
   if (p.dtype == HA_BF16)
-    attn_merge<__nv_bfloat16><<<dim3(rows, p.H), 128, 0, st>>>(
+    attn_merge<__nv_bfloat16><<<dim3(rows, p.H), 128, S * sizeof(float), st>>>(
         o_part, lse_part, S, p.H, p.d, static_cast<__nv_bfloat16*>(o), lse);
   else
-    attn_merge<float><<<dim3(rows, p.H), 128, 0, st>>>(o_part, lse_part, S, p.H, p.d,
-                                                       static_cast<float*>(o), lse);
+    attn_merge<float><<<dim3(rows, p.H), 128, S * sizeof(float), st>>>(
+        o_part, lse_part, S, p.H, p.d, static_cast<float*>(o), lse);
   return launched(cudaGetLastError());
 }
 

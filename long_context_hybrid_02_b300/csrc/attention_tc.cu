@@ -8,35 +8,46 @@
 // One shared K/V head serves every query head (MQA), so for one query row the
 // scores of a 64-head group are a GEMM with the keys as the M dimension:
 //   S^T[key, h] = sum_c K[key, c] q[h, c]            (M = 128 keys, N = 64, K = 512)
-//   O^T[c, h]  += sum_key V[key, c] P[key, h]         (M = 128 dims x 4, N = 64, K = keys)
+//   O^T[c, h]  += sum_key V[key, c] P[key, h]         (M = 128 dims x 4, N = 64, K = 128)
 // Both MMAs read 128-byte-swizzled shared-memory tiles: K and q are K-major, V
 // and P are MN-major (the row of 64 dims / 64 heads is contiguous), so the very
 // same gathered key rows serve as the A operand of both products.
 //
-// Work item = (query row, 64-head group, key split): at most kMaxTiles tiles of
-// 128 slots of the row's key list
+// Work item = (query row, 64-head group, key split): a range of slots of the
+// row's key list, in tiles of 128 slots,
 //   slots [0, n_c)          compressed entries idx[slot] (CSA) or slot (HCA),
-//   slots [n_c, n_c + n_w)  window positions t-n_w+1 .. t,
-// so the exact softmax of the split is taken over scores held in tensor memory
-// (no online rescaling).  A split writes its normalised output and log-sum-exp
-// as a float32 partial that attn_merge combines in split order, or the final
-// bfloat16 output when the row has one split.
+//   slots [n_c, n_c + n_w)  window positions t-n_w+1 .. t.
+// The softmax is streamed over the tiles: per head a reference maximum m (log2
+// units) is kept and raised only when a tile's maximum exceeds it by more than
+// kRescaleLog2; then O^T (in tensor memory) and the running sums are scaled by
+// exp2(m_old - m_new) before the tile's P.V is added.  P = exp2(c*s - m) <= 2^8
+// is stored as bfloat16; o = O / l with l the sum of the stored P values, which
+// is the exact softmax whatever m is.
 //
-// Persistent CTA (one per SM), warp-specialised:
-//   warps 0-3  producer: gathers each tile's key rows with 16-byte cp.async into a
-//              ring of kRing 32 KiB stages (per 64-dim block: 128 K rows + the 64
-//              q rows; then per 128-dim block: 128 V rows), warming L2 with every
-//              gathered row first;
-//   warp 4     MMA issuer (one thread): S tiles, then O^T 128 dims at a time into
-//              one of two tensor-memory accumulators;
-//   warps 5-8  softmax: per-head max and sum over every tile of the item (TMEM
-//              lane = key), P written as bfloat16 into shared memory;
-//   warps 9-12 epilogue: O^T from tensor memory, scaled by 1/l, to global memory.
+// Warp-specialised CTA (9 warps):
+//   warps 0-3  producer: q of the item into a resident buffer, then the key rows
+//              of each tile, K one tile ahead of V, with 16-byte cp.async into a
+//              ring of kRing 32 KiB stages (warp w fills every stage g with
+//              g % kRing == w and blocks only on its own copies; empty slots are
+//              zero-filled);
+//   warp 4     MMA issuer (one thread): S(t+1) into the second score buffer while
+//              the softmax works on S(t), then P(t).V(t);
+//   warps 5-8  softmax of each tile (TMEM lane = key), O^T rescaling, and at the
+//              end of the item the epilogue (TMEM lane = head dim).
+// Rows with one split: persistent grid (one CTA per SM) looping over items.  Rows
+// with 2..8 splits: one item per CTA and the splits of a row form a thread-block
+// cluster; every CTA sends each head dim of its normalised o to the CTA that owns
+// that dim with remote shared-memory stores, and every CTA merges its dims (no
+// workspace, no second launch).
 // Every wait is bounded (tc::kWaitLimitNs); on timeout the kernel records an error
 // code in the library's device error word and returns.
+#include <cooperative_groups.h>
+
 #include "common.cuh"
 #include "kernels.h"
 #include "tc.cuh"
+
+namespace cg = cooperative_groups;
 
 namespace ha {
 namespace {
@@ -46,30 +57,27 @@ using bf16 = __nv_bfloat16;
 constexpr int kD = 512;                          // head dim handled
 constexpr int kHG = 64;                          // heads per item (N of both MMAs)
 constexpr int kTile = 128;                       // key slots per tile (M of the score MMA)
-constexpr int kMaxTiles = 5;                     // tiles per item
-constexpr int kRing = 4;                         // shared-memory stages
-constexpr int kStageBytes = 32768;
-constexpr int kKBlockBytes = kTile * 128;        // 128 key rows x 64 dims
-constexpr int kPTileBytes = kTile * kHG * 2;     // 128 keys x 64 heads
-constexpr int kThreads = 13 * 32;
+constexpr int kRing = 4;                         // shared-memory stages (one per producer warp)
+constexpr int kStageBytes = 32768;               // 128 key rows x 128 dims
+constexpr int kHalfBytes = kTile * 128;          // 128 key rows x 64 dims
+constexpr int kQBytes = kHG * kD * 2;            // 64 heads x 512 dims
+constexpr int kPBytes = kTile * kHG * 2;         // 128 keys x 64 heads
+constexpr int kThreads = 9 * 32;
 constexpr int kTmemCols = 512;
-constexpr int kSCol = 0;                         // S tiles: columns [0, 64 * kMaxTiles)
-constexpr int kOCol = 64 * kMaxTiles;            // O^T double buffer: 2 x 64 columns
-static_assert(kOCol + 2 * kHG <= kTmemCols, "tensor memory budget");
+constexpr int kSCol = 0;                         // two S buffers: columns [0, 128)
+constexpr int kOCol = 2 * kHG;                   // O^T: 4 x 64 columns [128, 384)
 constexpr int kTokFlag = 1 << 30;                // slot code: per-token row
+constexpr int kMaxClusterSplits = 8;             // splits merged inside the kernel
+constexpr float kRescaleLog2 = 8.f;              // P <= 2^8 before the reference moves
 
 constexpr size_t kSmemRing = size_t(kRing) * kStageBytes;
-constexpr size_t kSmemP = size_t(kMaxTiles) * kPTileBytes;
-constexpr size_t kSmemMisc = 4 * 64 * 4 + 64 * 4 + 2 * 128 * 4 + 32 * 8 + 16;
-constexpr size_t kSmemUsed = 1024 + kSmemRing + kSmemP + kSmemMisc;
-// The whole 227 KiB is requested (one CTA per SM either way): every operand read
-// the descriptors can address, even with the leading / stride offsets exchanged,
-// then stays inside the CTA's shared memory.
-constexpr size_t kSmem = 232448;
-static_assert(kSmemUsed <= kSmem, "shared-memory budget");
-// farthest byte of the last P tile's last K step if LBO (16 KiB) were taken as SBO
-static_assert(1023 + kSmemRing + (kMaxTiles - 1) * kPTileBytes + 7 * 2048 + kKBlockBytes + 1024 <=
-                  kSmem, "descriptor reach");
+constexpr size_t kSmemTbl = size_t(4) * 2 * kTile * 4;           // [warp][tile parity][128]
+constexpr size_t kSmemMisc = (4 * 64 + 64 + 64 + 2 * 64) * 4 + 32 * 8 + 16;
+constexpr size_t kSmem = 1024 + kQBytes + kSmemRing + kPBytes + kSmemTbl + kSmemMisc;
+static_assert(kSmem <= 232448, "shared-memory budget");
+// receive buffer of the in-cluster merge: [8 splits][64 heads][64 dims] .. [3][64][172]
+static_assert(3 * 64 * 172 * 4 <= kSmemRing + kPBytes && 7 * 64 * 76 * 4 <= kSmemRing + kPBytes,
+              "merge buffer");
 
 struct TcArgs {
   const bf16* q;         // [rows, H, 512]
@@ -82,11 +90,10 @@ struct TcArgs {
   int decode, Tq, H, n_cap, tok_cap, n_win, m, k, elig;
   float c;               // softmax scale * log2(e)
   int S, kps, HG;
-  long long n_items;     // rows * S * HG
-  bf16* o;               // [rows, H, 512]         (S == 1)
-  float* lse;            // [rows, H] or null      (S == 1)
-  float* o_part;         // [rows, S, H, 512]      (S > 1)
-  float* lse_part;       // [rows, S, H]
+  int cluster_merge;     // 1: one item per CTA, splits of a row merged in the cluster
+  long long n_items;     // rows * HG * S
+  bf16* o;               // [rows, H, 512]
+  float* lse;            // [rows, H] or null
   int* err;
 };
 
@@ -101,10 +108,10 @@ struct Item {
 
 __device__ __forceinline__ Item item_of(const TcArgs& a, long long it) {
   Item x;
-  x.hg = int(it % a.HG);
-  const long long rest = it / a.HG;
-  x.split = int(rest % a.S);
-  x.r = int(rest / a.S);
+  x.split = int(it % a.S);
+  const long long rest = it / a.S;
+  x.hg = int(rest % a.HG);
+  x.r = int(rest / a.HG);
   x.b = x.r / a.Tq;
   x.t = a.decode ? a.pos[x.b] - 1 : a.pos[x.r];
   x.ne = x.t >= 0 ? n_eligible(x.t, a.n_win, a.m, a.elig, a.n_cap) : 0;
@@ -117,14 +124,20 @@ __device__ __forceinline__ Item item_of(const TcArgs& a, long long it) {
   return x;
 }
 
-// Row of the key in `slot`: -1 none; else b*n_cap + j (compressed entry j) or
-// (b*tok_cap + token slot) | kTokFlag (window position).
-__device__ __forceinline__ int slot_code(const TcArgs& a, const Item& x, int slot) {
+// Entry named by compressed slot `slot` (< n_c): idx[r, slot] (CSA) or slot (HCA).
+// The load is unconditional on a clamped address, so that a loop over slots
+// issues all of its loads before the first use.
+__device__ __forceinline__ int slot_entry(const TcArgs& a, const Item& x, int slot) {
+  if (!a.idx) return slot;
+  const int s = min(max(slot, 0), a.k - 1);
+  return __ldg(a.idx + (long long)x.r * a.k + s);
+}
+
+// Row of the key in `slot` given its entry j (ignored for window slots): -1 none;
+// else b*n_cap + j (compressed entry j) or (b*tok_cap + token slot) | kTokFlag.
+__device__ __forceinline__ int slot_code(const TcArgs& a, const Item& x, int slot, int j) {
   if (slot < x.lo || slot >= x.hi) return -1;
-  if (slot < x.n_c) {
-    const int j = a.idx ? __ldg(a.idx + (long long)x.r * a.k + slot) : slot;
-    return (j >= 0 && j < x.ne) ? x.b * a.n_cap + j : -1;
-  }
+  if (slot < x.n_c) return (j >= 0 && j < x.ne) ? x.b * a.n_cap + j : -1;
   const int u = x.t - x.n_w + 1 + (slot - x.n_c);
   return (x.b * a.tok_cap + u % a.tok_cap) | kTokFlag;
 }
@@ -148,43 +161,39 @@ __device__ __forceinline__ bool named_barrier_all(int id, int count, bool v) {
   return r != 0;
 }
 
-// 64 values per lane -> lane L holds op-reductions over the warp of values 2L, 2L+1.
+// 32 values per lane -> the op-reduction over the warp of value L, returned to lane L
+// (31 shuffles: each step exchanges half of the remaining values).
 template <typename Op>
-__device__ __forceinline__ void warp_transpose_reduce64(const float (&v)[64], float& r0,
-                                                        float& r1, Op op) {
+__device__ __forceinline__ float warp_transpose_reduce32(const float (&v)[32], Op op) {
   const int lane = threadIdx.x & 31;
-  float a[32], b[16], c[8], d[4];
+  float a[16], b[8], c[4], d[2];
   bool hi = lane & 16;
 #pragma unroll
-  for (int i = 0; i < 32; ++i) {
-    const float send = hi ? v[i] : v[i + 32], keep = hi ? v[i + 32] : v[i];
+  for (int i = 0; i < 16; ++i) {
+    const float send = hi ? v[i] : v[i + 16], keep = hi ? v[i + 16] : v[i];
     a[i] = op(keep, __shfl_xor_sync(0xffffffffu, send, 16));
   }
   hi = lane & 8;
 #pragma unroll
-  for (int i = 0; i < 16; ++i) {
-    const float send = hi ? a[i] : a[i + 16], keep = hi ? a[i + 16] : a[i];
+  for (int i = 0; i < 8; ++i) {
+    const float send = hi ? a[i] : a[i + 8], keep = hi ? a[i + 8] : a[i];
     b[i] = op(keep, __shfl_xor_sync(0xffffffffu, send, 8));
   }
   hi = lane & 4;
 #pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    const float send = hi ? b[i] : b[i + 8], keep = hi ? b[i + 8] : b[i];
+  for (int i = 0; i < 4; ++i) {
+    const float send = hi ? b[i] : b[i + 4], keep = hi ? b[i + 4] : b[i];
     c[i] = op(keep, __shfl_xor_sync(0xffffffffu, send, 4));
   }
   hi = lane & 2;
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const float send = hi ? c[i] : c[i + 4], keep = hi ? c[i + 4] : c[i];
+  for (int i = 0; i < 2; ++i) {
+    const float send = hi ? c[i] : c[i + 2], keep = hi ? c[i + 2] : c[i];
     d[i] = op(keep, __shfl_xor_sync(0xffffffffu, send, 2));
   }
   hi = lane & 1;
-  {
-    const float send0 = hi ? d[0] : d[2], keep0 = hi ? d[2] : d[0];
-    const float send1 = hi ? d[1] : d[3], keep1 = hi ? d[3] : d[1];
-    r0 = op(keep0, __shfl_xor_sync(0xffffffffu, send0, 1));
-    r1 = op(keep1, __shfl_xor_sync(0xffffffffu, send1, 1));
-  }
+  const float send = hi ? d[0] : d[1], keep = hi ? d[1] : d[0];
+  return op(keep, __shfl_xor_sync(0xffffffffu, send, 1));
 }
 
 struct MaxOp { __device__ float operator()(float x, float y) const { return fmaxf(x, y); } };
@@ -194,38 +203,37 @@ __global__ void __launch_bounds__(kThreads, 1) attn_decode_tc(const TcArgs a) {
   extern __shared__ unsigned char smem_raw[];
   unsigned char* base = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  unsigned char* ring = base;
+  unsigned char* sQ = base;                                  // 8 blocks x (64 heads x 128 B)
+  unsigned char* ring = sQ + kQBytes;
   unsigned char* sP = ring + kSmemRing;
-  float* red = reinterpret_cast<float*>(sP + kSmemP);   // [4 warps][64]
-  float* fin = red + 4 * 64;                             // [64] log2-scaled max
-  float* stats = fin + 64;                               // [2 items][inv_l 64 | lse 64]
-  uint64_t* full = reinterpret_cast<uint64_t*>(stats + 2 * 128);
+  int* tbl_all = reinterpret_cast<int*>(sP + kPBytes);       // [4 warps][2][128]
+  float* red = reinterpret_cast<float*>(tbl_all + 4 * 2 * kTile);   // [4 warps][64]
+  float* mref = red + 4 * 64;                                // [64] reference max (log2 units)
+  float* alpha = mref + 64;                                  // [64] rescale of this tile
+  float* stats = alpha + 64;                                 // [inv_l 64 | lse 64]
+  uint64_t* full = reinterpret_cast<uint64_t*>(stats + 2 * 64);
   uint64_t* empty = full + kRing;
-  uint64_t* s_full = empty + kRing;
-  uint64_t* p_full = s_full + 1;
-  uint64_t* p_empty = p_full + 1;
-  uint64_t* o_full = p_empty + 1;     // [2]
-  uint64_t* o_empty = o_full + 2;     // [2]
-  uint64_t* st_full = o_empty + 2;    // [2]
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(st_full + 2);
+  uint64_t* q_full = empty + kRing;
+  uint64_t* q_empty = q_full + 1;
+  uint64_t* s_full = q_empty + 1;     // [2]
+  uint64_t* s_empty = s_full + 2;     // [2]
+  uint64_t* p_full = s_empty + 2;
+  uint64_t* pv_done = p_full + 1;
+  uint64_t* o_empty = pv_done + 1;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(o_empty + 1);
+  int* rescale_flag = reinterpret_cast<int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kRing; ++s) { tc::mbar_init(&full[s], 128); tc::mbar_init(&empty[s], 1); }
-    tc::mbar_init(s_full, 1);
+    for (int s = 0; s < kRing; ++s) { tc::mbar_init(&full[s], 32); tc::mbar_init(&empty[s], 1); }
+    tc::mbar_init(q_full, 128);
+    tc::mbar_init(q_empty, 1);
+    for (int i = 0; i < 2; ++i) { tc::mbar_init(&s_full[i], 1); tc::mbar_init(&s_empty[i], 128); }
     tc::mbar_init(p_full, 128);
-    tc::mbar_init(p_empty, 1);
-    for (int i = 0; i < 2; ++i) {
-      tc::mbar_init(&o_full[i], 1);
-      tc::mbar_init(&o_empty[i], 128);
-      tc::mbar_init(&st_full[i], 32);
-    }
+    tc::mbar_init(pv_done, 1);
+    tc::mbar_init(o_empty, 128);
     tc::fence_mbar_init();
   }
-  // Rows a tile does not load keep their previous (finite) contents; start from zeros.
-  for (int i = threadIdx.x; i < int((kSmemRing + kSmemP) / 16); i += kThreads)
-    reinterpret_cast<uint4*>(ring)[i] = make_uint4(0, 0, 0, 0);
-  tc::fence_proxy_async_smem();
   if (warp == 4) { tc::tmem_alloc(tmem_slot, kTmemCols); tc::tmem_relinquish(); }
   tc::fence_before_sync();
   __syncthreads();
@@ -234,269 +242,411 @@ __global__ void __launch_bounds__(kThreads, 1) attn_decode_tc(const TcArgs a) {
 
   if (warp < 4) {
     // ------------------------------------------------------------------ producer
+    static_assert(kRing == 4, "one producer warp per ring stage");
+    const int w = warp;                       // fills the stages g with g % kRing == w
     const int pt = threadIdx.x;               // 0..127
-    const int rbase = pt >> 3, ch = pt & 7;   // rows rbase + 16 i, 16-byte chunk ch
-    const uint32_t swz = uint32_t((ch ^ (rbase & 7)) << 4);
-    long long g = 0, arrived = 0;
+    const int rsub = lane >> 3, ch = lane & 7;   // rows rsub + 4 i, 16-byte chunk ch
+    const uint32_t stage = tc::smem_u32(ring + size_t(w) * kStageBytes);
+    const uint32_t q_base = tc::smem_u32(sQ);
+    long long g = 0, n = 0;
     bool ok = true;
-    auto acquire = [&](uint32_t& sa) -> bool {
-      const int s = int(g % kRing);
-      if (!tc::mbar_wait(&empty[s], uint32_t(((g / kRing) & 1) ^ 1), a.err, 41)) return false;
-      sa = tc::smem_u32(ring + size_t(s) * kStageBytes);
-      return true;
+    auto put = [&](uint32_t dst, int code, const bf16* comp, const bf16* tok, int col) {
+      if (code >= 0)
+        tc::cp_async16(dst, key_row(comp, tok, code) + col);
+      else
+        asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(dst), "r"(0) : "memory");
     };
-    auto release = [&]() {
+    bool q_pending = false;                   // q copies committed, not yet published
+    auto publish = [&](uint64_t* bar) {
       tc::cp_async_commit();
-      ++g;
-      if (g - arrived > kRing - 1) {
-        tc::cp_async_wait<kRing - 1>();
+      if (q_pending) {                        // the q group is the older one
+        tc::cp_async_wait<1>();
         tc::fence_proxy_async_smem();
-        tc::mbar_arrive(&full[arrived % kRing]);
-        ++arrived;
+        tc::mbar_arrive(q_full);
+        q_pending = false;
       }
+      tc::cp_async_wait<0>();
+      tc::fence_proxy_async_smem();
+      tc::mbar_arrive(bar);
     };
-    for (long long it = blockIdx.x; it < a.n_items && ok; it += gridDim.x) {
+    for (long long it = blockIdx.x; it < a.n_items && ok; it += gridDim.x, ++n) {
       const Item x = item_of(a, it);
-      int code[kMaxTiles][8];
+      // stages: K(0); then per tile t: K(t+1), V(t).  A warp touches every tile (each
+      // run of 4 stages holds one of its stages) and keeps that tile's row table.
+      auto k_stages = [&](int t) -> bool {
+        int* tbl = tbl_all + (w * 2 + (t & 1)) * kTile;
+        __syncwarp();
+        int ent[kTile / 32];
 #pragma unroll
-      for (int t = 0; t < kMaxTiles; ++t)
+        for (int j = 0; j < kTile / 32; ++j) ent[j] = slot_entry(a, x, x.lo + t * kTile + lane + 32 * j);
 #pragma unroll
-        for (int i = 0; i < 8; ++i)
-          code[t][i] = t < x.nt ? slot_code(a, x, x.lo + t * kTile + rbase + 16 * i) : -1;
-      const bf16* qrow = a.q + ((long long)x.r * a.H + x.hg * kHG) * kD;
-      // scores: per tile, 8 blocks of 64 dims (K rows + q rows)
-      for (int t = 0; t < x.nt && ok; ++t) {
-        if (ch == 0) {
+        for (int j = 0; j < kTile / 32; ++j)
+          tbl[lane + 32 * j] = slot_code(a, x, x.lo + t * kTile + lane + 32 * j, ent[j]);
+        __syncwarp();
+        for (int pair = 0; pair < 4; ++pair, ++g) {
+          if (int(g % kRing) != w) continue;
+          if (!tc::mbar_wait(&empty[w], uint32_t(((g / kRing) & 1) ^ 1), a.err, 41)) return false;
+          // 8 rows at a time: their codes in registers first (the copies are asm
+          // statements with a memory clobber; table reads between them would be
+          // serialised), then 16 copies
+#pragma unroll 1
+          for (int i0 = 0; i0 < kTile / 4; i0 += 8) {
+            int cd[8];
 #pragma unroll
-          for (int i = 0; i < 8; ++i)
-            if (code[t][i] >= 0) {
-              tc::prefetch_l2(key_row(a.ck, a.k_tok, code[t][i]), kD * 2);
-              tc::prefetch_l2(key_row(a.cv, a.v_tok, code[t][i]), kD * 2);
+            for (int u = 0; u < 8; ++u) cd[u] = tbl[rsub + 4 * (i0 + u)];
+#pragma unroll
+            for (int hb = 0; hb < 2; ++hb) {
+              const int kb = 2 * pair + hb;
+#pragma unroll
+              for (int u = 0; u < 8; ++u) {
+                const int row = rsub + 4 * (i0 + u);
+                put(stage + hb * kHalfBytes + row * 128 + ((ch ^ (row & 7)) << 4), cd[u], a.ck,
+                    a.k_tok, kb * 64 + ch * 8);
+              }
             }
+          }
+          publish(&full[w]);
         }
-        for (int kb = 0; kb < kD / 64; ++kb) {
-          uint32_t sa;
-          if (!(ok = acquire(sa))) break;
+        return true;
+      };
+      auto v_stages = [&](int t) -> bool {
+        const int* tbl = tbl_all + (w * 2 + (t & 1)) * kTile;
+        for (int mb = 0; mb < kD / 128; ++mb, ++g) {
+          if (int(g % kRing) != w) continue;
+          if (!tc::mbar_wait(&empty[w], uint32_t(((g / kRing) & 1) ^ 1), a.err, 42)) return false;
+#pragma unroll 1
+          for (int i0 = 0; i0 < kTile / 4; i0 += 8) {
+            int cd[8];
 #pragma unroll
-          for (int i = 0; i < 8; ++i)
-            if (code[t][i] >= 0)
-              tc::cp_async16(sa + (rbase + 16 * i) * 128 + swz,
-                             key_row(a.ck, a.k_tok, code[t][i]) + kb * 64 + ch * 8);
+            for (int u = 0; u < 8; ++u) cd[u] = tbl[rsub + 4 * (i0 + u)];
 #pragma unroll
-          for (int i = 0; i < 4; ++i)
-            tc::cp_async16(sa + kKBlockBytes + (rbase + 16 * i) * 128 + swz,
-                           qrow + (long long)(rbase + 16 * i) * kD + kb * 64 + ch * 8);
-          release();
+            for (int u = 0; u < 8; ++u) {
+              const int row = rsub + 4 * (i0 + u);
+              const uint32_t off = row * 128 + ((ch ^ (row & 7)) << 4);
+              put(stage + off, cd[u], a.cv, a.v_tok, mb * 128 + ch * 8);
+              put(stage + kHalfBytes + off, cd[u], a.cv, a.v_tok, mb * 128 + 64 + ch * 8);
+            }
+          }
+          publish(&full[w]);
         }
+        return true;
+      };
+      // q of the item: every warp copies a quarter, once the previous item's score
+      // MMAs are done with the buffer; its copies stay in flight (their own group)
+      // while the first tile's table is built, and are published before the first
+      // stage of this warp
+      if (!(ok = tc::mbar_wait(q_empty, uint32_t((n & 1) ^ 1), a.err, 40))) break;
+      const bf16* qrow = a.q + ((long long)x.r * a.H + x.hg * kHG) * kD;
+#pragma unroll
+      for (int i = 0; i < kQBytes / 16 / 128; ++i) {   // 32 chunks per thread
+        const int c = pt + 128 * i;
+        const int kb = c >> 9, h = (c >> 3) & 63;
+        tc::cp_async16(q_base + kb * (kHG * 128) + h * 128 + ((ch ^ (h & 7)) << 4),
+                       qrow + (long long)h * kD + kb * 64 + ch * 8);
       }
-      // values: per 128-dim block, every tile
-      for (int mb = 0; mb < kD / 128 && ok; ++mb) {
-        for (int t = 0; t < x.nt; ++t) {
-          uint32_t sa;
-          if (!(ok = acquire(sa))) break;
-#pragma unroll
-          for (int cb = 0; cb < 2; ++cb)
-#pragma unroll
-            for (int i = 0; i < 8; ++i)
-              if (code[t][i] >= 0)
-                tc::cp_async16(sa + cb * kKBlockBytes + (rbase + 16 * i) * 128 + swz,
-                               key_row(a.cv, a.v_tok, code[t][i]) + mb * 128 + cb * 64 + ch * 8);
-          release();
-        }
+      tc::cp_async_commit();
+      q_pending = true;
+      if (!(ok = k_stages(0))) break;
+      for (int t = 0; t < x.nt && ok; ++t) {
+        if (t + 1 < x.nt && !(ok = k_stages(t + 1))) break;
+        ok = v_stages(t);
       }
     }
     tc::cp_async_wait<0>();
-    tc::fence_proxy_async_smem();
-    if (ok)
-      while (arrived < g) { tc::mbar_arrive(&full[arrived % kRing]); ++arrived; }
   } else if (warp == 4) {
     // ------------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       constexpr uint32_t idesc_s = tc::idesc_bf16_f32(kTile, kHG);
       constexpr uint32_t idesc_o = tc::idesc_bf16_f32(128, kHG, true, true);
-      const uint32_t p_base = tc::smem_u32(sP);
-      long long g = 0, n = 0, ob = 0;
+      const uint32_t q_base = tc::smem_u32(sQ), p_base = tc::smem_u32(sP);
+      long long g = 0, n = 0, G = 0;   // stage, item and global tile counters
       bool ok = true;
+      // S(tile Gt) from its 4 K stages into score buffer Gt & 1
+      auto s_mma = [&](long long Gt) -> bool {
+        const int buf = int(Gt & 1);
+        if (!tc::mbar_wait(&s_empty[buf], uint32_t(((Gt >> 1) & 1) ^ 1), a.err, 43)) return false;
+        tc::fence_after_sync();
+        for (int pair = 0; pair < 4; ++pair, ++g) {
+          const int s = int(g % kRing);
+          if (!tc::mbar_wait(&full[s], uint32_t((g / kRing) & 1), a.err, 44)) return false;
+          tc::fence_after_sync();
+          const uint32_t sa = tc::smem_u32(ring + size_t(s) * kStageBytes);
+#pragma unroll
+          for (int hb = 0; hb < 2; ++hb)
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+              const int kb = 2 * pair + hb;
+              tc::mma_bf16(tmem + kSCol + buf * kHG,
+                           tc::sdesc_kmajor_sw128(sa + hb * kHalfBytes + kk * 32),
+                           tc::sdesc_kmajor_sw128(q_base + kb * (kHG * 128) + kk * 32), idesc_s,
+                           (kb | kk) != 0 ? 1u : 0u);
+            }
+          tc::mma_commit(&empty[s]);
+        }
+        tc::mma_commit(&s_full[buf]);
+        return true;
+      };
       for (long long it = blockIdx.x; it < a.n_items && ok; it += gridDim.x, ++n) {
         const Item x = item_of(a, it);
-        for (int t = 0; t < x.nt && ok; ++t)
-          for (int kb = 0; kb < kD / 64; ++kb, ++g) {
-            const int s = int(g % kRing);
-            if (!(ok = tc::mbar_wait(&full[s], uint32_t((g / kRing) & 1), a.err, 42))) break;
-            tc::fence_after_sync();
-            const uint32_t sa = tc::smem_u32(ring + size_t(s) * kStageBytes);
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk)
-              tc::mma_bf16(tmem + kSCol + t * kHG, tc::sdesc_kmajor_sw128(sa + kk * 32),
-                           tc::sdesc_kmajor_sw128(sa + kKBlockBytes + kk * 32), idesc_s,
-                           (kb | kk) != 0 ? 1u : 0u);
-            tc::mma_commit(&empty[s]);
-          }
-        if (!ok) break;
-        tc::mma_commit(s_full);
-        if (!(ok = tc::mbar_wait(p_full, uint32_t(n & 1), a.err, 43))) break;
+        if (!(ok = tc::mbar_wait(q_full, uint32_t(n & 1), a.err, 45))) break;
         tc::fence_after_sync();
-        for (int mb = 0; mb < kD / 128 && ok; ++mb, ++ob) {
-          const int buf = int(ob & 1);
-          if (!(ok = tc::mbar_wait(&o_empty[buf], uint32_t(((ob >> 1) & 1) ^ 1), a.err, 44))) break;
+        if (!(ok = s_mma(G))) break;
+        if (x.nt == 1) tc::mma_commit(q_empty);
+        for (int t = 0; t < x.nt && ok; ++t, ++G) {
+          if (t + 1 < x.nt) {
+            if (!(ok = s_mma(G + 1))) break;
+            if (t + 2 == x.nt) tc::mma_commit(q_empty);
+          }
+          if (!(ok = tc::mbar_wait(p_full, uint32_t(G & 1), a.err, 46))) break;
+          if (t == 0 && !(ok = tc::mbar_wait(o_empty, uint32_t((n & 1) ^ 1), a.err, 47))) break;
           tc::fence_after_sync();
-          for (int t = 0; t < x.nt; ++t, ++g) {
+          for (int mb = 0; mb < kD / 128 && ok; ++mb, ++g) {
             const int s = int(g % kRing);
-            if (!(ok = tc::mbar_wait(&full[s], uint32_t((g / kRing) & 1), a.err, 45))) break;
+            if (!(ok = tc::mbar_wait(&full[s], uint32_t((g / kRing) & 1), a.err, 48))) break;
             tc::fence_after_sync();
             const uint32_t sa = tc::smem_u32(ring + size_t(s) * kStageBytes);
-            const uint32_t pa = p_base + t * kPTileBytes;
 #pragma unroll
             for (int kk = 0; kk < kTile / 16; ++kk)
-              tc::mma_bf16(tmem + kOCol + buf * kHG,
-                           tc::sdesc_sw128(sa + kk * 2048, kKBlockBytes, 1024),
-                           tc::sdesc_sw128(pa + kk * 2048, kKBlockBytes, 1024), idesc_o,
+              tc::mma_bf16(tmem + kOCol + mb * kHG,
+                           tc::sdesc_sw128(sa + kk * 2048, kHalfBytes, 1024),
+                           tc::sdesc_sw128(p_base + kk * 2048, kHalfBytes, 1024), idesc_o,
                            (t | kk) != 0 ? 1u : 0u);
             tc::mma_commit(&empty[s]);
           }
-          if (ok) tc::mma_commit(&o_full[buf]);
+          if (ok) tc::mma_commit(pv_done);
         }
-        if (ok) tc::mma_commit(p_empty);
       }
     }
-  } else if (warp < 9) {
-    // ------------------------------------------------------------------ softmax
+  } else {
+    // ------------------------------------------------------------------ softmax + epilogue
     const int sw = warp - 5;                  // 0..3
     const int quarter = warp & 3;             // TMEM lanes 32*quarter ..
-    const int row = quarter * 32 + lane;      // key slot within a tile
+    const int row = quarter * 32 + lane;      // key slot within a tile / head dim within 128
     const uint32_t t_lane = uint32_t(quarter * 32) << 16;
     unsigned char* prow = sP + row * 128;
     const int rsw = row & 7;
-    long long n = 0;
-    for (long long it = blockIdx.x; it < a.n_items; it += gridDim.x, ++n) {
+    long long n = 0, G = 0;
+    bool ok = true;
+    for (long long it = blockIdx.x; it < a.n_items && ok; it += gridDim.x, ++n) {
       const Item x = item_of(a, it);
-      bool w = tc::mbar_wait(p_empty, uint32_t((n & 1) ^ 1), a.err, 51);
-      w = w && tc::mbar_wait(s_full, uint32_t(n & 1), a.err, 52);
-      if (!named_barrier_all(1, 128, w)) break;
-      tc::fence_after_sync();
-      unsigned vmask = 0;
-      for (int t = 0; t < x.nt; ++t)
-        if (slot_code(a, x, x.lo + t * kTile + row) >= 0) vmask |= 1u << t;
-      // pass 1: per-head maximum over the item's keys
-      float mx[64];
-#pragma unroll
-      for (int h = 0; h < 64; ++h) mx[h] = -INFINITY;
-      for (int t = 0; t < x.nt; ++t) {
+      // this warp's share of the per-head sums of P: heads lane and 32 + lane
+      float lw[2] = {0.f, 0.f};
+      for (int t = 0; t < x.nt; ++t, ++G) {
+        const int ent = slot_entry(a, x, x.lo + t * kTile + row);
+        const bool valid = slot_code(a, x, x.lo + t * kTile + row, ent) >= 0;
+        const int buf = int(G & 1);
+        bool wok = tc::mbar_wait(&s_full[buf], uint32_t((G >> 1) & 1), a.err, 51);
+        if (!(ok = named_barrier_all(1, 128, wok))) break;
+        tc::fence_after_sync();
+        // tile maximum per head
 #pragma unroll
         for (int half = 0; half < 2; ++half) {
           float v[32];
-          tc::tmem_ld32(tmem + t_lane + kSCol + t * kHG + half * 32, v);
-          if ((vmask >> t) & 1) {
+          tc::tmem_ld32(tmem + t_lane + kSCol + buf * kHG + half * 32, v);
+          if (!valid) {
 #pragma unroll
-            for (int h = 0; h < 32; ++h) mx[half * 32 + h] = fmaxf(mx[half * 32 + h], v[h]);
+            for (int h = 0; h < 32; ++h) v[h] = -INFINITY;
           }
+          red[sw * 64 + half * 32 + lane] = warp_transpose_reduce32(v, MaxOp());
         }
-      }
-      {
-        float r0, r1;
-        warp_transpose_reduce64(mx, r0, r1, MaxOp());
-        red[sw * 64 + 2 * lane] = r0;
-        red[sw * 64 + 2 * lane + 1] = r1;
-      }
-      tc::named_barrier(1, 128);
-      if (sw == 0) {
+        tc::named_barrier(1, 128);
+        if (sw == 0) {
+          bool moved = false;
 #pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          const int h = 2 * lane + e;
-          const float m = fmaxf(fmaxf(red[h], red[64 + h]), fmaxf(red[128 + h], red[192 + h]));
-          fin[h] = m == -INFINITY ? -INFINITY : m * a.c;
+          for (int e = 0; e < 2; ++e) {
+            const int h = 2 * lane + e;
+            const float tm = fmaxf(fmaxf(red[h], red[64 + h]), fmaxf(red[128 + h], red[192 + h]));
+            const float cand = tm == -INFINITY ? -INFINITY : tm * a.c;
+            const float old = t == 0 ? -INFINITY : mref[h];
+            float al = 1.f;
+            if (old == -INFINITY) {
+              mref[h] = cand;                 // nothing accumulated yet for this head
+            } else if (cand > old + kRescaleLog2) {
+              mref[h] = cand;
+              al = tc::ex2_approx(old - cand);
+              moved = true;
+            }
+            alpha[h] = al;
+          }
+          moved = __any_sync(0xffffffffu, moved);
+          if (lane == 0) *rescale_flag = moved ? 1 : 0;
         }
-      }
-      tc::named_barrier(1, 128);
-      // pass 2: P = exp2(c * s - m) as bfloat16, row sums of the rounded values
-      float l[64];
+        tc::named_barrier(1, 128);
+        // P of the previous tile must be consumed (and O final) before P / O change
+        if (G > 0) {
+          wok = tc::mbar_wait(pv_done, uint32_t((G - 1) & 1), a.err, 52);
+          if (!(ok = named_barrier_all(1, 128, wok))) break;
+          tc::fence_after_sync();
+        }
+        if (*rescale_flag) {
+          // O^T lane = head dim, column = head: scale column h by alpha[h]
+#pragma unroll 1
+          for (int half = 0; half < 2; ++half) {
+            float al[32];
 #pragma unroll
-      for (int h = 0; h < 64; ++h) l[h] = 0.f;
-      for (int t = 0; t < x.nt; ++t) {
-        const bool valid = (vmask >> t) & 1;
+            for (int h = 0; h < 32; ++h) al[h] = alpha[half * 32 + h];
+#pragma unroll 1
+            for (int mb = 0; mb < kD / 128; ++mb) {
+              float v[32];
+              const uint32_t col = tmem + t_lane + kOCol + mb * kHG + half * 32;
+              tc::tmem_ld32(col, v);
+#pragma unroll
+              for (int h = 0; h < 32; ++h) v[h] *= al[h];
+              tc::tmem_st32(col, v);
+            }
+          }
+          tc::tmem_wait_st();
+          lw[0] *= alpha[lane];
+          lw[1] *= alpha[32 + lane];
+        }
+        // P = exp2(c * s - m) as bfloat16, sums of the rounded values
 #pragma unroll
         for (int half = 0; half < 2; ++half) {
           float v[32];
-          tc::tmem_ld32(tmem + t_lane + kSCol + t * kHG + half * 32, v);
+          tc::tmem_ld32(tmem + t_lane + kSCol + buf * kHG + half * 32, v);
           uint32_t pk[16];
 #pragma unroll
           for (int h = 0; h < 32; h += 2) {
-            const float p0 = valid ? exp2f(v[h] * a.c - fin[half * 32 + h]) : 0.f;
-            const float p1 = valid ? exp2f(v[h + 1] * a.c - fin[half * 32 + h + 1]) : 0.f;
+            const float p0 = valid ? tc::ex2_approx(v[h] * a.c - mref[half * 32 + h]) : 0.f;
+            const float p1 = valid ? tc::ex2_approx(v[h + 1] * a.c - mref[half * 32 + h + 1]) : 0.f;
             const __nv_bfloat162 b2 = __floats2bfloat162_rn(p0, p1);
-            l[half * 32 + h] += __low2float(b2);
-            l[half * 32 + h + 1] += __high2float(b2);
+            v[h] = __low2float(b2);           // the rounded values are the ones summed
+            v[h + 1] = __high2float(b2);
             pk[h / 2] = *reinterpret_cast<const uint32_t*>(&b2);
           }
 #pragma unroll
           for (int j = 0; j < 4; ++j)
-            *reinterpret_cast<uint4*>(prow + t * kPTileBytes + (((half * 4 + j) ^ rsw) << 4)) =
+            *reinterpret_cast<uint4*>(prow + (((half * 4 + j) ^ rsw) << 4)) =
                 make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+          lw[half] += warp_transpose_reduce32(v, AddOp());
         }
+        tc::fence_proxy_async_smem();
+        tc::fence_before_sync();
+        tc::mbar_arrive(&s_empty[buf]);
+        tc::mbar_arrive(p_full);
       }
-      tc::fence_proxy_async_smem();
-      tc::fence_before_sync();
-      tc::mbar_arrive(p_full);
-      {
-        float r0, r1;
-        warp_transpose_reduce64(l, r0, r1, AddOp());
-        red[sw * 64 + 2 * lane] = r0;
-        red[sw * 64 + 2 * lane + 1] = r1;
-      }
-      tc::named_barrier(1, 128);
+      if (!ok) break;
+      // ---- epilogue of the item: sums over the four warps, then O^T / l
+      red[sw * 64 + lane] = lw[0];
+      red[sw * 64 + 32 + lane] = lw[1];
+      bool wok = tc::mbar_wait(pv_done, uint32_t((G - 1) & 1), a.err, 53);
+      if (!(ok = named_barrier_all(1, 128, wok))) break;
+      tc::fence_after_sync();
       if (sw == 0) {
-        float* st = stats + (n & 1) * 128;
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
           const int h = 2 * lane + e;
           const float sum = (red[h] + red[64 + h]) + (red[128 + h] + red[192 + h]);
-          st[h] = sum > 0.f ? 1.f / sum : 0.f;
-          st[64 + h] = sum > 0.f ? (fin[h] + log2f(sum)) * 0.69314718055994531f : -INFINITY;
+          stats[h] = sum > 0.f ? 1.f / sum : 0.f;
+          stats[64 + h] = sum > 0.f ? (mref[h] + log2f(sum)) * 0.69314718055994531f : -INFINITY;
         }
-        tc::mbar_arrive(&st_full[n & 1]);
+      }
+      tc::named_barrier(1, 128);
+      if (a.cluster_merge) break;             // the only item: O^T leaves after the cluster barrier
+      const long long hrow = (long long)x.r * a.H + x.hg * kHG;   // first head of the group
+      // 1/l of the 32 heads of a half in registers before any store (the stores
+      // could otherwise alias them and serialise every load)
+#pragma unroll 1
+      for (int half = 0; half < 2; ++half) {
+        float sc[32];
+#pragma unroll
+        for (int h = 0; h < 32; ++h) sc[h] = stats[half * 32 + h];
+#pragma unroll 1
+        for (int mb = 0; mb < kD / 128; ++mb) {
+          const int dd = mb * 128 + row;
+          float v[32];
+          tc::tmem_ld32(tmem + t_lane + kOCol + mb * kHG + half * 32, v);
+          bf16* dst = a.o + (hrow + half * 32) * kD + dd;
+#pragma unroll
+          for (int h = 0; h < 32; ++h) dst[(long long)h * kD] = __float2bfloat16_rn(v[h] * sc[h]);
+        }
+      }
+      if (sw < 2 && a.lse) a.lse[hrow + sw * 32 + lane] = stats[64 + sw * 32 + lane];
+      tc::fence_before_sync();
+      tc::mbar_arrive(o_empty);
+      tc::named_barrier(1, 128);              // stats and mref are rewritten by the next item
+    }
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  if (a.cluster_merge) {
+    // Every CTA of the cluster holds one split of the same query row and head group.
+    // CTA r owns the head dims [lo(r), lo(r + 1)), lo(r) = 4 * floor(128 r / S).
+    // After a first barrier (every CTA's ring is idle), each CTA sends its
+    // normalised o, dim by dim, to the owner of the dim and its lse to everyone,
+    // with remote shared-memory stores; after a second barrier each CTA merges
+    // its dims in split order:
+    //   o = sum_s exp(lse_s - mx) o_s / sum_s exp(lse_s - mx),  lse = mx + log(sum).
+    cg::cluster_group cluster = cg::this_cluster();
+    const Item x = item_of(a, blockIdx.x);
+    const int S = a.S, me = x.split;
+    const int W = ((kD + S - 1) / S + 3) / 4 * 4;            // row width of the receive buffer
+    float* recv = reinterpret_cast<float*>(ring);             // [S][64 heads][W]
+    float* lse_in = reinterpret_cast<float*>(tbl_all);        // [S][64]
+    float* wts = lse_in + kMaxClusterSplits * kHG;            // [S][64]
+    cluster.sync();
+    if (warp >= 5) {
+      const int sw = warp - 5, quarter = warp & 3, row = quarter * 32 + lane;
+      const uint32_t t_lane = uint32_t(quarter * 32) << 16;
+#pragma unroll 1
+      for (int half = 0; half < 2; ++half) {
+        float sc[32];
+#pragma unroll
+        for (int h = 0; h < 32; ++h) sc[h] = stats[half * 32 + h];
+#pragma unroll 1
+        for (int mb = 0; mb < kD / 128; ++mb) {
+          const int dd = mb * 128 + row;
+          const int r = ((dd >> 2) * S + S - 1) / 128;      // owner of dim dd
+          const int off = dd - 4 * (r * 128 / S);
+          float* dst = cluster.map_shared_rank(recv, r) + (me * kHG + half * 32) * W + off;
+          float v[32];
+          tc::tmem_ld32(tmem + t_lane + kOCol + mb * kHG + half * 32, v);
+#pragma unroll
+          for (int h = 0; h < 32; ++h) dst[h * W] = v[h] * sc[h];
+        }
+      }
+      if (sw < 2) {
+        const float l = stats[64 + sw * 32 + lane];
+        for (int r = 0; r < S; ++r) cluster.map_shared_rank(lse_in, r)[me * kHG + sw * 32 + lane] = l;
       }
     }
-  } else {
-    // ------------------------------------------------------------------ epilogue
-    const int quarter = warp & 3;
-    const uint32_t t_lane = uint32_t(quarter * 32) << 16;
-    const int e = (warp - 9) * 32 + lane;     // 0..127
-    long long n = 0, ob = 0;
-    bool ok = true;
-    for (long long it = blockIdx.x; it < a.n_items && ok; it += gridDim.x, ++n) {
-      const Item x = item_of(a, it);
-      if (!(ok = tc::mbar_wait(&st_full[n & 1], uint32_t((n >> 1) & 1), a.err, 61))) break;
-      const float* st = stats + (n & 1) * 128;
-      const long long hrow = (long long)x.r * a.H + x.hg * kHG;   // first head of the group
-      for (int mb = 0; mb < kD / 128; ++mb, ++ob) {
-        const int buf = int(ob & 1);
-        if (!(ok = tc::mbar_wait(&o_full[buf], uint32_t((ob >> 1) & 1), a.err, 62))) break;
-        tc::fence_after_sync();
-        const int dd = mb * 128 + quarter * 32 + lane;
-#pragma unroll
-        for (int half = 0; half < 2; ++half) {
-          float v[32];
-          tc::tmem_ld32(tmem + t_lane + kOCol + buf * kHG + half * 32, v);
-          if (a.S == 1) {
-#pragma unroll
-            for (int h = 0; h < 32; ++h)
-              a.o[(hrow + half * 32 + h) * kD + dd] = __float2bfloat16_rn(v[h] * st[half * 32 + h]);
-          } else {
-            float* dst = a.o_part + (((long long)x.r * a.S + x.split) * a.H + x.hg * kHG) * kD + dd;
-#pragma unroll
-            for (int h = 0; h < 32; ++h) dst[(long long)(half * 32 + h) * kD] = v[h] * st[half * 32 + h];
-          }
-        }
-        tc::fence_before_sync();
-        tc::mbar_arrive(&o_empty[buf]);
+    cluster.sync();                                           // every piece has arrived
+    float* inv = stats;                                       // [64]
+    const int h0 = x.hg * kHG;
+    if (threadIdx.x < kHG) {
+      const int h = threadIdx.x;
+      float mx = -INFINITY;
+      for (int s2 = 0; s2 < S; ++s2) mx = fmaxf(mx, lse_in[s2 * kHG + h]);
+      float tot = 0.f;
+      for (int s2 = 0; s2 < S; ++s2) {
+        const float wv = mx == -INFINITY ? 0.f : expf(lse_in[s2 * kHG + h] - mx);
+        wts[s2 * kHG + h] = wv;
+        tot += wv;
       }
-      if (ok && e < kHG) {
-        if (a.S == 1) {
-          if (a.lse) a.lse[hrow + e] = st[64 + e];
-        } else {
-          a.lse_part[((long long)x.r * a.S + x.split) * a.H + x.hg * kHG + e] = st[64 + e];
-        }
+      inv[h] = tot > 0.f ? 1.f / tot : 0.f;
+      if (me == 0 && a.lse) a.lse[(long long)x.r * a.H + h0 + h] = tot > 0.f ? mx + logf(tot) : -INFINITY;
+    }
+    __syncthreads();
+    const int g_lo = me * (kD / 4) / S, g_hi = (me + 1) * (kD / 4) / S;
+    const int width = g_hi - g_lo;                            // 4-dim groups of this CTA
+    for (int i = threadIdx.x; i < kHG * width; i += kThreads) {
+      const int h = i / width, g4 = i % width;
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int s2 = 0; s2 < S; ++s2) {
+        const float wv = wts[s2 * kHG + h];
+        const float4 v = *reinterpret_cast<const float4*>(recv + (s2 * kHG + h) * W + 4 * g4);
+        acc.x = fmaf(wv, v.x, acc.x);
+        acc.y = fmaf(wv, v.y, acc.y);
+        acc.z = fmaf(wv, v.z, acc.z);
+        acc.w = fmaf(wv, v.w, acc.w);
       }
+      const float iv = inv[h];
+      const __nv_bfloat162 lo2 = __floats2bfloat162_rn(acc.x * iv, acc.y * iv);
+      const __nv_bfloat162 hi2 = __floats2bfloat162_rn(acc.z * iv, acc.w * iv);
+      uint2 pk;
+      pk.x = *reinterpret_cast<const uint32_t*>(&lo2);
+      pk.y = *reinterpret_cast<const uint32_t*>(&hi2);
+      *reinterpret_cast<uint2*>(a.o + ((long long)x.r * a.H + h0 + h) * kD + 4 * (g_lo + g4)) = pk;
     }
   }
   tc::fence_before_sync();
@@ -528,11 +678,10 @@ bool attention_tc_supported(const ha_params& p, int n_cap, int tok_cap) {
 AttnPlan plan_attention_tc(const ha_params& p, int rows, int max_keys) {
   AttnPlan pl{};
   const long long units = (long long)rows * (p.H / kHG);
-  const int per_item = kMaxTiles * kTile;
-  const int s_min = (max_keys + per_item - 1) / per_item;
   const int sms = num_sms();
+  // enough splits to cover the SMs, at most what one cluster merges
   int S = units >= sms ? 1 : int(sms / units);
-  if (S < s_min) S = s_min;
+  if (S > kMaxClusterSplits) S = kMaxClusterSplits;
   if (S < 1) S = 1;
   int kps = (max_keys + S - 1) / S;
   kps = (kps + 15) / 16 * 16;
@@ -542,7 +691,7 @@ AttnPlan plan_attention_tc(const ha_params& p, int rows, int max_keys) {
   pl.n_splits = S;
   pl.keys_per_split = kps;
   pl.tile = kTile;
-  pl.ws_bytes = S > 1 ? size_t(rows) * S * p.H * (p.d + 1) * sizeof(float) + 256 : 0;
+  pl.ws_bytes = 0;                                      // splits merge inside the kernel
   return pl;
 }
 
@@ -577,18 +726,28 @@ cudaError_t launch_attention_tc(const ha_params& p, const AttnPlan& pl, int deco
   a.n_items = (long long)rows * a.S * a.HG;
   a.o = static_cast<bf16*>(o);
   a.lse = lse;
-  if (a.S > 1) {
-    a.o_part = static_cast<float*>(ws);
-    a.lse_part = a.o_part + size_t(rows) * a.S * p.H * p.d;
-  }
   a.err = err;
+  a.cluster_merge = a.S > 1 ? 1 : 0;
+  (void)ws;
   cudaError_t e = ensure_smem(reinterpret_cast<const void*>(attn_decode_tc), kSmem);
   if (e != cudaSuccess) return e;
-  const long long grid = a.n_items < num_sms() ? a.n_items : num_sms();
-  attn_decode_tc<<<unsigned(grid), kThreads, kSmem, st>>>(a);
-  e = launched(cudaGetLastError());
-  if (e != cudaSuccess || a.S == 1) return e;
-  return launch_attn_merge(p, rows, a.S, a.o_part, a.lse_part, o, lse, st);
+  cudaLaunchConfig_t cfg = {};
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = kSmem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  if (a.cluster_merge) {
+    cfg.gridDim = dim3(unsigned(a.n_items));               // one item per CTA
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = unsigned(a.S);
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+  } else {
+    cfg.gridDim = dim3(unsigned(a.n_items < num_sms() ? a.n_items : num_sms()));
+  }
+  return launched(cudaLaunchKernelEx(&cfg, attn_decode_tc, a));
 }
 
 }  // namespace ha

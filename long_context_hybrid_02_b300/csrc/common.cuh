@@ -80,10 +80,11 @@ __device__ __forceinline__ int n_eligible(int t, int n_win, int m, int elig, int
 }
 
 // Order-preserving key of a float score for top-k: larger score -> larger key,
-// NaN ranks like -inf.
+// NaN ranks like -inf, -0 and +0 are the same score (a tie, broken by index).
 __device__ __forceinline__ uint32_t score_key(float s) {
   uint32_t u = __float_as_uint(s);
   if (s != s) u = 0xff800000u;  // NaN -> -inf
+  if (s == 0.f) u = 0u;         // -0 -> +0
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 

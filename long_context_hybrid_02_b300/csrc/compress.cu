@@ -9,7 +9,7 @@
 // threads read consecutive chunks of the same token row, so each warp issues
 // fully coalesced 512-byte requests.  Accumulation is float32 in token order.
 //   m <= 16 : one thread per (block, chunk) walks all m tokens.
-//   m  > 16 : the block's tokens are split into G = min(16, ceil(m/8)) contiguous
+//   m  > 16 : the block's tokens are split into G = min(8, ceil(m/8)) contiguous
 //             groups; the G partial sums of a chunk are added in group order
 //             through shared memory, so the result does not depend on scheduling.
 #include "common.cuh"
@@ -51,28 +51,40 @@ __global__ void __launch_bounds__(256) compress_small_m(CompressArgs a) {
     int tsr, chunk;
     locate<T>(a, c, tsr, chunk);
     const int row_elems = a.chunks[tsr] * V;
+    // the block's rows and gates are loaded together (neither depends on the other)
+    const T* src = static_cast<const T*>(a.src[tsr]);
+    uint4 raw[16];
     float g[16];
-    float gmax = -INFINITY;
-    for (int i = 0; i < a.m; ++i) {
-      const long long u = (long long)j * a.m + i;
-      g[i] = a.gate[(long long)b * a.tok_cap + u % a.tok_cap];
-      gmax = fmaxf(gmax, g[i]);
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      if (i < a.m) {
+        const long long u = (long long)j * a.m + i;
+        const long long slot = (long long)b * a.tok_cap + u % a.tok_cap;
+        raw[i] = ld16(src + slot * row_elems + chunk * V);
+        g[i] = a.gate[slot];
+      }
     }
+    float gmax = -INFINITY;
+#pragma unroll
+    for (int i = 0; i < 16; ++i)
+      if (i < a.m) gmax = fmaxf(gmax, g[i]);
     float den = 0.f;
-    for (int i = 0; i < a.m; ++i) { g[i] = expf(g[i] - gmax); den += g[i]; }
+#pragma unroll
+    for (int i = 0; i < 16; ++i)
+      if (i < a.m) { g[i] = expf(g[i] - gmax); den += g[i]; }
     const float inv = 1.f / den;
     float acc[V];
 #pragma unroll
     for (int e = 0; e < V; ++e) acc[e] = 0.f;
-    const T* src = static_cast<const T*>(a.src[tsr]);
-    for (int i = 0; i < a.m; ++i) {
-      const long long u = (long long)j * a.m + i;
-      const T* row = src + ((long long)b * a.tok_cap + u % a.tok_cap) * row_elems;
-      float f[V];
-      unpack(ld16(row + chunk * V), f);
-      const float al = g[i] * inv;
 #pragma unroll
-      for (int e = 0; e < V; ++e) acc[e] = fmaf(al, f[e], acc[e]);
+    for (int i = 0; i < 16; ++i) {
+      if (i < a.m) {
+        float f[V];
+        unpack(raw[i], f);
+        const float al = g[i] * inv;
+#pragma unroll
+        for (int e = 0; e < V; ++e) acc[e] = fmaf(al, f[e], acc[e]);
+      }
     }
     T* dst = static_cast<T*>(a.dst[tsr]) + ((long long)b * a.n_cap + j) * row_elems;
     st16(dst + chunk * V, pack(acc));
@@ -82,7 +94,7 @@ __global__ void __launch_bounds__(256) compress_small_m(CompressArgs a) {
 // CTA = (block task, slice of kSlice chunks) x G token groups.
 constexpr int kSlice = 64;
 constexpr int kBatch = 8;        // loads in flight per thread
-constexpr int kMaxGroups = 16;
+constexpr int kMaxGroups = 8;
 
 __host__ __device__ inline int n_groups(int m) {
   const int g = (m + kBatch - 1) / kBatch;
@@ -90,7 +102,7 @@ __host__ __device__ inline int n_groups(int m) {
 }
 
 template <typename T>
-__global__ void __launch_bounds__(1024) compress_large_m(CompressArgs a) {
+__global__ void __launch_bounds__(512) compress_large_m(CompressArgs a) {
   constexpr int V = Elem<T>::kVec;
   extern __shared__ float sm[];                    // alpha[m] | partial[G][kSlice][V]
   const int G = n_groups(a.m);
@@ -105,6 +117,21 @@ __global__ void __launch_bounds__(1024) compress_large_m(CompressArgs a) {
   const int grp = threadIdx.x / kSlice;             // token group
   const long long base_u = (long long)j * a.m;
 
+  // the first batch of this thread's rows is requested before the gate softmax
+  const int c = blockIdx.y * kSlice + lane_c;       // chunk over all tensors
+  const int total_chunks = a.chunks[0] + a.chunks[1] + a.chunks[2];
+  int tsr = 0, chunk = 0, row_elems = 0;
+  const T* src = nullptr;
+  const int i_beg = grp * per_group, i_end = min(a.m, (grp + 1) * per_group);
+  uint4 raw[kBatch];
+  if (c < total_chunks) {
+    locate<T>(a, c, tsr, chunk);
+    row_elems = a.chunks[tsr] * V;
+    src = static_cast<const T*>(a.src[tsr]) + (long long)b * a.tok_cap * row_elems;
+#pragma unroll
+    for (int i = 0; i < kBatch; ++i)
+      if (i_beg + i < i_end) raw[i] = ld16(src + ((base_u + i_beg + i) % a.tok_cap) * row_elems + chunk * V);
+  }
   // gate softmax of this block (warp 0, fixed order)
   if (threadIdx.x < 32) {
     float mx = -INFINITY;
@@ -124,22 +151,16 @@ __global__ void __launch_bounds__(1024) compress_large_m(CompressArgs a) {
   }
   __syncthreads();
 
-  const int c = blockIdx.y * kSlice + lane_c;       // chunk over all tensors
-  const int total_chunks = a.chunks[0] + a.chunks[1] + a.chunks[2];
   float acc[V];
 #pragma unroll
   for (int e = 0; e < V; ++e) acc[e] = 0.f;
-  int tsr = 0, chunk = 0, row_elems = 0;
   if (c < total_chunks) {
-    locate<T>(a, c, tsr, chunk);
-    row_elems = a.chunks[tsr] * V;
-    const T* src = static_cast<const T*>(a.src[tsr]) + (long long)b * a.tok_cap * row_elems;
-    const int i_end = min(a.m, (grp + 1) * per_group);
-    for (int i0 = grp * per_group; i0 < i_end; i0 += kBatch) {
-      uint4 raw[kBatch];
+    for (int i0 = i_beg; i0 < i_end; i0 += kBatch) {
+      if (i0 != i_beg) {
 #pragma unroll
-      for (int i = 0; i < kBatch; ++i)
-        if (i0 + i < i_end) raw[i] = ld16(src + ((base_u + i0 + i) % a.tok_cap) * row_elems + chunk * V);
+        for (int i = 0; i < kBatch; ++i)
+          if (i0 + i < i_end) raw[i] = ld16(src + ((base_u + i0 + i) % a.tok_cap) * row_elems + chunk * V);
+      }
 #pragma unroll
       for (int i = 0; i < kBatch; ++i) {
         if (i0 + i < i_end) {

@@ -2,28 +2,51 @@
 // compressed entries are attended, k = 512 for V4-Flash and 1024 for V4-Pro).
 //
 // Exact radix select over order-preserving 32-bit keys of the float scores (NaN
-// ranks as -inf).  One CTA of 1024 threads per row:
-//   1. four passes over 8-bit digits, most significant first, build a histogram of
-//      the keys that still match the selected prefix (warp-aggregated shared-memory
-//      atomics through __match_any_sync) and pick the digit holding the k-th
-//      largest key -> the threshold key T and how many keys equal to T are needed;
-//   2. one pass in ascending index order keeps every key > T and the first
-//      `need` keys == T (block-wide prefix sums of warp ballots), which realises
-//      the tie rule "larger score, then smaller index" and writes the result in
-//      ascending index order without a sort.
-// Rows of up to kSmemKeys keys are held in shared memory; longer rows are re-read
-// from global memory (L2) on every pass.
+// ranks as -inf).  A row is handled by a thread-block cluster of C CTAs (C = 1
+// when there are enough rows to fill the GPU); CTA r of the cluster holds the
+// keys of segment r of the row in shared memory.
+//   1. three passes over 11-, 11- and 10-bit digits, most significant first: every
+//      CTA histograms the keys of its segment that still match the selected prefix
+//      (warp-aggregated shared-memory atomics), the C histograms are summed over
+//      distributed shared memory, and every CTA picks the same digit holding the
+//      k-th largest key -> the threshold key T and how many keys equal to T are
+//      needed (`need_eq`);
+//   2. one ordered pass keeps every key > T and the first need_eq keys == T in
+//      index order, which realises the tie rule "larger score, then smaller index"
+//      and writes the result in ascending index order without a sort: each warp
+//      owns a contiguous run of its CTA's segment, counts, and after a block scan
+//      and a cluster-wide exchange of the per-CTA counts writes its selections at
+//      their final positions.
+// Segments longer than the shared-memory budget are re-read from global memory
+// (L2) on every pass.
+#include <cooperative_groups.h>
+
 #include "common.cuh"
 #include "kernels.h"
+
+namespace cg = cooperative_groups;
 
 namespace ha {
 namespace {
 
-constexpr int kThreads = 1024;
-constexpr int kSmemKeys = 48 * 1024;
+constexpr int kThreads = 512;
+constexpr int kWarps = kThreads / 32;
+constexpr int kBins = 2048;
+constexpr int kMaxCluster = 8;
+constexpr int kSmemKeys = 40 * 1024;      // keys held in shared memory per CTA
 
-// Exclusive prefix sum of v over the CTA; returns the prefix, total in *total.
-__device__ __forceinline__ int block_exclusive_scan(int v, int* warp_tot, int* total) {
+struct TopkShared {
+  int hist[kBins];          // this CTA's histogram of the current pass
+  int hsum[2][kBins];       // cluster-wide histogram, by pass parity
+  int warp_a[kWarps + 1];   // scan scratch
+  int warp_b[kWarps + 1];
+  int sel_digit, sel_above;
+  int cnt_gt, cnt_eq;       // this CTA's counts of keys > T and == T
+};
+
+// Inclusive scan of v over the CTA (kThreads threads); returns the inclusive prefix
+// and the total in *total.  `scratch` holds kWarps + 1 ints.
+__device__ __forceinline__ int block_inclusive_scan(int v, int* scratch, int* total) {
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
   int x = v;
 #pragma unroll
@@ -31,116 +54,167 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int* warp_tot, int* t
     const int y = __shfl_up_sync(0xffffffffu, x, o);
     if (lane >= o) x += y;
   }
-  if (lane == 31) warp_tot[wid] = x;
+  if (lane == 31) scratch[wid] = x;
   __syncthreads();
   if (wid == 0) {
-    int t = warp_tot[lane];
+    const int t = lane < kWarps ? scratch[lane] : 0;
     int s = t;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
       const int y = __shfl_up_sync(0xffffffffu, s, o);
       if (lane >= o) s += y;
     }
-    warp_tot[lane] = s - t;                 // exclusive prefix of warp totals
-    if (lane == 31) warp_tot[32] = s;
+    if (lane < kWarps) scratch[lane] = s - t;   // exclusive prefix of warp totals
+    if (lane == kWarps - 1) scratch[kWarps] = s;
   }
   __syncthreads();
-  const int res = warp_tot[wid] + x - v;
-  *total = warp_tot[32];
-  __syncthreads();                          // warp_tot reusable after return
+  const int res = scratch[wid] + x;
+  *total = scratch[kWarps];
+  __syncthreads();
   return res;
 }
 
-__global__ void __launch_bounds__(kThreads) topk_rows(const float* __restrict__ scores, int n_cap,
-                                                      const int32_t* __restrict__ q_pos, int k,
-                                                      int n_win, int m, int elig,
-                                                      int32_t* __restrict__ idx) {
+__global__ void __launch_bounds__(kThreads) topk_cluster(const float* __restrict__ scores,
+                                                         int n_cap, const int32_t* __restrict__ q_pos,
+                                                         int k, int n_win, int m, int elig,
+                                                         int seg_len, int32_t* __restrict__ idx) {
   extern __shared__ uint32_t skeys[];
-  __shared__ int hist[256];
-  __shared__ int warp_tot[33];
-  __shared__ int sel_digit, sel_above;
-  if (threadIdx.x == 0) { sel_digit = 0; sel_above = 0; }
-  const int row = blockIdx.x;
-  const int t = q_pos[row];
-  const int n = n_eligible(t, n_win, m, elig, n_cap);
+  __shared__ TopkShared sh;
+  cg::cluster_group cluster = cg::this_cluster();
+  const int C = int(cluster.num_blocks());
+  const int rank = int(cluster.block_rank());
+  const int row = blockIdx.x / C;
+  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+  const int n = n_eligible(q_pos[row], n_win, m, elig, n_cap);
   int32_t* out = idx + (long long)row * k;
-  if (n <= k) {
-    for (int i = threadIdx.x; i < k; i += kThreads) out[i] = i < n ? i : -1;
+  if (n <= k) {                                   // uniform over the cluster
+    if (rank == 0)
+      for (int i = tid; i < k; i += kThreads) out[i] = i < n ? i : -1;
     return;
   }
   const float* s = scores + (long long)row * n_cap;
-  const bool in_smem = n <= kSmemKeys;
-  if (in_smem) {
-    for (int i = threadIdx.x; i < n; i += kThreads) skeys[i] = score_key(s[i]);
-    __syncthreads();
-  }
-  auto key_at = [&](int i) -> uint32_t { return in_smem ? skeys[i] : score_key(__ldg(s + i)); };
+  const int lo = min(n, rank * seg_len), hi = min(n, lo + seg_len);
+  const int len = hi - lo;
+  const bool in_smem = len <= kSmemKeys;
+  if (in_smem)
+    for (int i = tid; i < len; i += kThreads) skeys[i] = score_key(s[lo + i]);
+  auto key_at = [&](int i) -> uint32_t { return in_smem ? skeys[i] : score_key(__ldg(s + lo + i)); };
 
   uint32_t prefix = 0, pmask = 0;
-  int remaining = k;                        // how many of the selected still to place
-  for (int pass = 0; pass < 4; ++pass) {
-    const int shift = 24 - 8 * pass;
-    for (int i = threadIdx.x; i < 256; i += kThreads) hist[i] = 0;
+  int remaining = k;                              // selected keys still to place
+  for (int i = tid; i < kBins; i += kThreads) sh.hsum[0][i] = 0;
+#pragma unroll 1
+  for (int pass = 0; pass < 3; ++pass) {
+    const int shift = pass == 0 ? 21 : (pass == 1 ? 10 : 0);
+    const uint32_t dmask = pass == 2 ? 0x3ffu : 0x7ffu;
+    int* hsum = sh.hsum[pass & 1];
+    // the other buffer was last read by this CTA's previous scan; peers add into it
+    // only after the next cluster barrier
+    for (int i = tid; i < kBins; i += kThreads) { sh.hist[i] = 0; sh.hsum[(pass + 1) & 1][i] = 0; }
     __syncthreads();
-    for (int base = 0; base < n; base += kThreads) {
-      const int i = base + threadIdx.x;
-      const bool valid = i < n;
+    for (int base = 0; base < len; base += kThreads) {
+      const int i = base + tid;
+      const bool valid = i < len;
       const uint32_t key = valid ? key_at(i) : 0u;
       const bool match = valid && ((key & pmask) == prefix);
       const unsigned act = __ballot_sync(0xffffffffu, match);
       if (match) {
-        const uint32_t digit = (key >> shift) & 0xffu;
+        const uint32_t digit = (key >> shift) & dmask;
         const unsigned peers = __match_any_sync(act, digit);
-        if ((threadIdx.x & 31) == __ffs(peers) - 1) atomicAdd(&hist[digit], __popc(peers));
+        if (lane == __ffs(peers) - 1) atomicAdd(&sh.hist[digit], __popc(peers));
       }
     }
-    __syncthreads();
-    if (threadIdx.x < 32) {
-      // lane l owns bins 255-8l .. 248-8l (descending); find the bin where the
-      // running count from the top reaches `remaining`
-      const int lane = threadIdx.x;
-      int c[8], tot = 0;
+    if (pass == 0) cluster.sync();                // every peer's hsum[0] is zeroed
+    else __syncthreads();
+    // add this CTA's non-zero bins into every peer's (and its own) sum
+    for (int b = tid; b < kBins; b += kThreads) {
+      const int v = sh.hist[b];
+      if (v != 0)
+        for (int c = 0; c < C; ++c) atomicAdd(cluster.map_shared_rank(hsum, c) + b, v);
+    }
+    cluster.sync();                               // every CTA holds the full histogram
+    // thread t owns bins 2047-4t .. 2044-4t (descending); find the bin where the
+    // running count from the top reaches `remaining`
+    int c4[4], own = 0;
 #pragma unroll
-      for (int q = 0; q < 8; ++q) { c[q] = hist[255 - 8 * lane - q]; tot += c[q]; }
-      int incl = tot;
+    for (int q = 0; q < 4; ++q) { c4[q] = hsum[kBins - 1 - 4 * tid - q]; own += c4[q]; }
+    int total;
+    const int incl = block_inclusive_scan(own, sh.warp_a, &total);
+    const int excl = incl - own;
+    if (excl < remaining && remaining <= incl) {
+      int run = excl;
 #pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int y = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += y;
-      }
-      const int excl = incl - tot;
-      if (excl < remaining && remaining <= incl) {
-        int run = excl;
-#pragma unroll
-        for (int q = 0; q < 8; ++q) {
-          if (run < remaining && remaining <= run + c[q]) { sel_digit = 255 - 8 * lane - q; sel_above = run; }
-          run += c[q];
+      for (int q = 0; q < 4; ++q) {
+        if (run < remaining && remaining <= run + c4[q]) {
+          sh.sel_digit = kBins - 1 - 4 * tid - q;
+          sh.sel_above = run;
         }
+        run += c4[q];
       }
     }
     __syncthreads();
-    prefix |= uint32_t(sel_digit) << shift;
-    pmask |= 0xffu << shift;
-    remaining -= sel_above;
+    prefix |= uint32_t(sh.sel_digit) << shift;
+    pmask |= dmask << shift;
+    remaining -= sh.sel_above;
     __syncthreads();
   }
-  // prefix is now the k-th largest key; `remaining` keys equal to it are taken.
+  // prefix is the k-th largest key; `remaining` keys equal to it are taken.
   const uint32_t thr = prefix;
   const int need_eq = remaining;
-  int eq_before = 0, out_before = 0;
-  for (int base = 0; base < n; base += kThreads) {
-    const int i = base + threadIdx.x;
-    const uint32_t key = i < n ? key_at(i) : 0u;
-    const int is_eq = (i < n && key == thr) ? 1 : 0;
-    int eq_tot;
-    const int eq_rank = eq_before + block_exclusive_scan(is_eq, warp_tot, &eq_tot);
-    const int take = (i < n && (key > thr || (is_eq && eq_rank < need_eq))) ? 1 : 0;
-    int take_tot;
-    const int pos = out_before + block_exclusive_scan(take, warp_tot, &take_tot);
-    if (take && pos < k) out[pos] = i;
-    eq_before += eq_tot;
-    out_before += take_tot;
+
+  // ordered pass: warp w owns the contiguous run [w*per_warp, (w+1)*per_warp) of the segment
+  const int per_warp = ((len + kWarps - 1) / kWarps + 31) / 32 * 32;
+  const int w_lo = min(len, wid * per_warp), w_hi = min(len, w_lo + per_warp);
+  int gt = 0, eq = 0;
+  for (int base = w_lo; base < w_hi; base += 32) {
+    const int i = base + lane;
+    const uint32_t key = i < w_hi ? key_at(i) : 0u;
+    gt += __popc(__ballot_sync(0xffffffffu, i < w_hi && key > thr));
+    eq += __popc(__ballot_sync(0xffffffffu, i < w_hi && key == thr));
   }
+  int gt_tot, eq_tot;
+  const int gt_incl = block_inclusive_scan(lane == 0 ? gt : 0, sh.warp_a, &gt_tot);
+  const int eq_incl = block_inclusive_scan(lane == 0 ? eq : 0, sh.warp_b, &eq_tot);
+  int gt_before = __shfl_sync(0xffffffffu, gt_incl, 0) - gt;   // within this CTA
+  int eq_before = __shfl_sync(0xffffffffu, eq_incl, 0) - eq;
+  if (tid == 0) { sh.cnt_gt = gt_tot; sh.cnt_eq = eq_tot; }
+  cluster.sync();
+  for (int c = 0; c < rank; ++c) {
+    const TopkShared* o = cluster.map_shared_rank(&sh, c);
+    gt_before += o->cnt_gt;
+    eq_before += o->cnt_eq;
+  }
+  for (int base = w_lo; base < w_hi; base += 32) {
+    const int i = base + lane;
+    const uint32_t key = i < w_hi ? key_at(i) : 0u;
+    const bool is_gt = i < w_hi && key > thr;
+    const bool is_eq = i < w_hi && key == thr;
+    const unsigned bgt = __ballot_sync(0xffffffffu, is_gt);
+    const unsigned beq = __ballot_sync(0xffffffffu, is_eq);
+    const unsigned below = (1u << lane) - 1u;
+    const int my_gt = gt_before + __popc(bgt & below);
+    const int my_eq = eq_before + __popc(beq & below);
+    const int taken_eq = min(my_eq, need_eq);    // equal keys taken before this one
+    if (is_gt) out[my_gt + taken_eq] = lo + i;
+    else if (is_eq && my_eq < need_eq) out[my_gt + my_eq] = lo + i;
+    gt_before += __popc(bgt);
+    eq_before += __popc(beq);
+  }
+  cluster.sync();                                 // keep shared memory alive for remote readers
+}
+
+int g_num_sms[64] = {};
+
+int num_sms() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+  if (g_num_sms[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+      n = 148;
+    g_num_sms[dev] = n;
+  }
+  return g_num_sms[dev];
 }
 
 }  // namespace
@@ -149,11 +223,31 @@ size_t topk_workspace_bytes(const ha_params&, int, int) { return 0; }
 
 cudaError_t launch_topk(const ha_params& p, const float* scores, int n_cap, const int32_t* q_pos,
                         int Tq, int32_t* idx, void*, size_t, cudaStream_t st) {
-  const size_t smem = size_t(n_cap < kSmemKeys ? n_cap : kSmemKeys) * sizeof(uint32_t);
-  cudaError_t e = ensure_smem(reinterpret_cast<const void*>(topk_rows), smem);
+  const long long rows = (long long)p.B * Tq;
+  // CTAs per row: enough to cover the GPU when rows are few, and enough for every
+  // segment to fit the shared-memory budget when possible.
+  int C = 1;
+  while (C < kMaxCluster && rows * C < num_sms()) C *= 2;
+  while (C < kMaxCluster && (n_cap + C - 1) / C > kSmemKeys) C *= 2;
+  const int seg_len = (n_cap + C - 1) / C;
+  const size_t smem = size_t(seg_len < kSmemKeys ? seg_len : kSmemKeys) * sizeof(uint32_t);
+  cudaError_t e = ensure_smem(reinterpret_cast<const void*>(topk_cluster), smem);
   if (e != cudaSuccess) return e;
-  topk_rows<<<p.B * Tq, kThreads, smem, st>>>(scores, n_cap, q_pos, p.k, p.n_win, p.m, p.elig, idx);
-  return launched(cudaGetLastError());
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(unsigned(rows * C));
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = unsigned(C);
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, topk_cluster, scores, n_cap, q_pos, p.k, p.n_win, p.m, p.elig,
+                         seg_len, idx);
+  return launched(e);
 }
 
 }  // namespace ha

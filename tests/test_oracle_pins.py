@@ -179,6 +179,13 @@ def test_topk_matches_heap_selection_with_ties_and_nan():
         assert got[got >= 0].tolist() == sorted(ref)
 
 
+def test_topk_signed_zeros_are_one_score():
+    # -0.0 == +0.0 as numbers, so they tie and the smaller index wins
+    s = np.array([-0.0, 0.0, -0.0, 0.0, -1.0])
+    assert O.topk_select(s, 2).tolist() == [0, 1]
+    assert O.topk_select(np.array([0.0, -0.0, 0.0]), 1).tolist() == [0]
+
+
 def test_topk_pads_when_fewer_than_k_and_handles_empty():
     assert O.topk_select(np.array([0.5, -1.0, 2.0]), 5).tolist() == [0, 1, 2, -1, -1]
     assert O.topk_select(np.array([]), 3).tolist() == [-1, -1, -1]

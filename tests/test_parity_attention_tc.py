@@ -186,3 +186,37 @@ def test_tc_decode_bitwise_repeatable_and_position_invariant():
     o2, l2 = _decode(p, q, ck, cv, n_cap, idx, k_tok, v_tok, L, ctx)
     assert torch.equal(o1, o2) and torch.equal(l1, l2)
     assert torch.equal(o1[0], o1[2]) and torch.equal(l1[0], l1[2])
+
+
+def test_tc_decode_hca_long_rows_need_more_than_eight_splits():
+    """6,144 + 128 keys per row: more splits than one cluster merges, so the split
+    partials go through the merge kernel."""
+    m, n_win, ring = 128, 128, 256
+    n_cap = 6144
+    L = n_cap * m
+    ctx = [L, L - 77]
+    Bn = len(ctx)
+    s = 1 / math.sqrt(D)
+    ck = synth.gaussian((Bn, n_cap, D), DEV, 400, s, torch.bfloat16)
+    cv = synth.gaussian((Bn, n_cap, D), DEV, 401, s, torch.bfloat16)
+    win_k = synth.gaussian((Bn, ring, D), DEV, 402, s, torch.bfloat16)   # positions L-256 .. L-1
+    win_v = synth.gaussian((Bn, ring, D), DEV, 403, s, torch.bfloat16)
+    k_ring = torch.empty_like(win_k)
+    v_ring = torch.empty_like(win_v)
+    pos = torch.arange(L - ring, L, device=DEV)
+    k_ring[:, pos % ring] = win_k
+    v_ring[:, pos % ring] = win_v
+    q = synth.gaussian((Bn, 64, D), DEV, 404, s, torch.bfloat16)
+    p = B.make_params(Bn, 64, D, n_win, m, 1, 1, 8, B.BF16)
+    o, lse = _decode(p, q, ck, cv, n_cap, None, k_ring, v_ring, ring,
+                     torch.tensor(ctx, dtype=torch.int32, device=DEV))
+    CK, CV = np64(ck), np64(cv)
+    for b, c in enumerate(ctx):
+        t = c - 1
+        ne = O.n_eligible(t, n_win, m)
+        win = O.window_positions(t, n_win)
+        keys = np.concatenate([CK[b, :ne], np64(win_k[b])[win - (L - ring)]])
+        vals = np.concatenate([CV[b, :ne], np64(win_v[b])[win - (L - ring)]])
+        ro, rl = O.attend(np64(q[b]), keys, vals, 1 / math.sqrt(D))
+        assert_close(np64(o[b]), ro, "bf16", f"o[{b}]")
+        assert_close(np64(lse[b]), rl, "bf16", f"lse[{b}]")

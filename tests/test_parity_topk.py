@@ -1,0 +1,105 @@
+"""csa_topk against the oracle's selection, bit-exact, in every launch configuration.
+
+The kernel splits a row over a cluster of up to 8 CTAs when rows are few, keeps
+each CTA's segment in shared memory up to 40,960 keys and re-reads longer
+segments from global memory, and uses one CTA per row when rows are many.  The
+scores are fed identically to both sides (float32), so the index sets must be
+identical: ties broken by the smaller index, NaN ranked as -inf, output in
+ascending index order with -1 padding.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+from long_context_hybrid_02_b300 import binding as B
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+def _run(scores, q_pos, k, m=4, n_win=128):
+    Bn, Tq, n_cap = scores.shape
+    p = B.make_params(Bn, 1, 512, n_win, m, k, 1, 8, B.F32)
+    idx = torch.full((Bn, Tq, k), -7, dtype=torch.int32, device=DEV)
+    nb = B.ha_workspace_size(p, B.OP_TOPK, Tq, n_cap, True)
+    ws = torch.empty(max(nb, 16), dtype=torch.uint8, device=DEV)
+    B.csa_topk(p, scores.to(DEV), n_cap, q_pos.to(DEV), Tq, idx, (ws.data_ptr(), ws.numel()))
+    torch.cuda.synchronize()
+    return idx.cpu().numpy()
+
+
+def _check(scores, q_pos, idx, k, m=4, n_win=128):
+    Bn, Tq, n_cap = scores.shape
+    for b in range(Bn):
+        for t in range(Tq):
+            ne = min(O.n_eligible(int(q_pos[b, t]), n_win, m), n_cap)
+            ref = O.topk_select(scores[b, t, :ne].double().numpy(), k)
+            assert idx[b, t].tolist() == ref.tolist(), (b, t, ne)
+
+
+def _scores(shape, seed, ties=None, nans=0):
+    g = torch.Generator().manual_seed(seed)
+    s = torch.randn(shape, generator=g)
+    if ties:
+        s = torch.round(s * ties) / ties
+    if nans:
+        flat = s.view(-1)
+        flat[torch.randperm(flat.numel(), generator=g)[:nans]] = float("nan")
+    return s
+
+
+def test_topk_million_token_rows_in_clusters():
+    """4 rows x 262,144 entries, k = 1024: 8-CTA clusters, 32,768 keys per CTA."""
+    n_cap, k = 262144, 1024
+    s = _scores((4, 1, n_cap), 1)
+    s[1] = torch.round(s[1] * 8) / 8                        # heavy ties
+    s[2, 0, ::7] = float("nan")
+    s[3, 0, :] = 0.5                                        # all equal
+    q_pos = torch.full((4, 1), 128 + 4 * n_cap - 1, dtype=torch.int32)
+    idx = _run(s, q_pos, k)
+    _check(s, q_pos, idx, k)
+
+
+def test_topk_segments_beyond_shared_memory():
+    """Segments of 50,000 keys (> 40,960): every radix pass re-reads global memory."""
+    n_cap, k = 400000, 512
+    s = _scores((2, 1, n_cap), 2, ties=16)
+    q_pos = torch.tensor([[128 + 4 * n_cap - 1], [128 + 4 * 300000 - 1]], dtype=torch.int32)
+    idx = _run(s, q_pos, k)
+    _check(s, q_pos, idx, k)
+
+
+def test_topk_many_rows_one_cta_each_ragged_eligibility():
+    """300 prefill rows (one CTA per row) with eligible counts from 0 to n_cap."""
+    n_cap, k = 5000, 512
+    rng = np.random.default_rng(3)
+    ne = rng.integers(0, n_cap + 1, 300)
+    ne[:4] = [0, 1, k, k + 1]
+    q_pos = torch.tensor((128 + 4 * ne - 1).reshape(1, 300), dtype=torch.int32)
+    q_pos[0, 0] = 5                                         # no eligible entry
+    s = _scores((1, 300, n_cap), 4, ties=4, nans=3000)
+    idx = _run(s, q_pos, k)
+    _check(s, q_pos, idx, k)
+
+
+@pytest.mark.parametrize("n_cap,k", [(700, 512), (16384, 512), (33792, 512), (8192, 1024)])
+def test_topk_decode_batches(n_cap, k):
+    s = _scores((32, 1, n_cap), 5 + n_cap, ties=32, nans=50)
+    q_pos = torch.full((32, 1), 128 + 4 * n_cap - 1, dtype=torch.int32)
+    q_pos[5, 0] = 128 + 4 * (k - 3) - 1                     # fewer eligible than k
+    idx = _run(s, q_pos, k)
+    _check(s, q_pos, idx, k)
+
+
+def test_topk_signed_zeros_tie():
+    """-0.0 and +0.0 are one score: the tie goes to the smaller index."""
+    n_cap, k = 2048, 512
+    s = torch.zeros((2, 1, n_cap))
+    s[0, 0, ::2] = -0.0                                     # alternate -0 / +0, all tied
+    s[1, 0, :300] = 1.0
+    s[1, 0, 300::3] = -0.0                                  # threshold at zero
+    q_pos = torch.full((2, 1), 128 + 4 * n_cap - 1, dtype=torch.int32)
+    idx = _run(s, q_pos, k)
+    _check(s, q_pos, idx, k)
+    assert idx[0, 0].tolist() == list(range(k))

@@ -26,8 +26,9 @@ A = 1 << 20      # aligned fake address: the refusal happens before any CUDA cal
 
 def test_static_decode_refuses_problems_beyond_the_fixed_scratch():
     B.load_library()
-    # 64 sequences x 128 heads x 512 dims over 8,192 + 128 keys needs ~1 GB of partials
-    p = B.make_params(64, 128, 512, 128, 128, dtype=B.BF16)
+    # float32 storage (the CUDA-core path splits every 128 keys): 64 sequences x 128
+    # heads x 512 dims over 8,192 + 128 keys needs ~1 GB of partials
+    p = B.make_params(64, 128, 512, 128, 128, dtype=B.F32)
     need = B.ha_workspace_size(p, B.OP_DECODE, 1, 8192, False)
     assert need > B.STATIC_SCRATCH_BYTES
     with pytest.raises(B.HAError) as e:
