@@ -7,9 +7,11 @@ sequence), top-512, indexer 64 heads x 128, bfloat16 storage, fp32 accumulation.
 One step = one decode token per sequence through the whole path: compress the
 block completed by the newest token, score every eligible entry, select the
 top-k, attend to selection + window (split-KV + merge).  The step's launches are
-captured once in a CUDA graph and replayed; timing uses CUDA events recorded
-inside the graph on the launching stream, with an L2 flush (256 MiB write)
-between timed steps.
+captured once in a CUDA graph and replayed; timing uses CUDA events recorded at
+both ends of the graph on the launching stream, with an L2 flush (256 MiB write,
+then 256 MiB read) before every timed step.  The library's kernels are chained
+with programmatic dependent launch, so the per-kernel breakdown comes from a
+second graph with an event between every two calls.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
 
@@ -317,62 +319,86 @@ def main():
                          device=dev)
     q = qry["q"][:, 0].contiguous()
     stream = torch.cuda.Stream(device=dev)
-    ev = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(5)]
     names = ["compress", "index", "topk", "attention"] if w.kind == "csa" else ["compress", "attention"]
+    n_ev = len(names) + 1
+    ev = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(n_ev)]
 
-    def step():
+    def step(marks: bool):
+        """One decode step.  The first and last events are always recorded; with
+        marks, also one between every two calls (the per-kernel breakdown: a
+        recorded event between two kernels also keeps the second from starting
+        early, so the headline graph has none)."""
         s = stream.cuda_stream
         ev[0].record(stream)
         layer.compress(new_blk, 1, s)
-        ev[1].record(stream)
+        if marks:
+            ev[1].record(stream)
         if w.kind == "csa":
             B.csa_index_scores(layer.p, qry["qI"], qry["w_idx"], layer.cki, layer.n_cap,
                                qry["q_pos"], 1, layer.scores, s)
-            ev[2].record(stream)
+            if marks:
+                ev[2].record(stream)
             B.csa_topk(layer.p, layer.scores, layer.n_cap, qry["q_pos"], 1, layer.idx,
                        (layer.ws.data_ptr(), layer.ws.numel()), s)
-            ev[3].record(stream)
+            if marks:
+                ev[3].record(stream)
             idx = layer.idx
         else:
             idx = None
         B.hybrid_attn_decode(layer.p, q, layer.ck, layer.cv, layer.n_cap, idx, tok["k_tok"],
                              tok["v_tok"], layer.tok_cap, qry["ctx_len"], layer.o, layer.lse,
                              (layer.ws.data_ptr(), layer.ws.numel()), s)
-        ev[4 if w.kind == "csa" else 2].record(stream)
+        ev[n_ev - 1].record(stream)
 
-    n_ev = len(names) + 1
-    # eager warm-up (sets kernel attributes), then capture
+    # eager warm-up (sets kernel attributes), then capture both graphs
     with torch.cuda.stream(stream):
-        step()
+        step(True)
     torch.cuda.synchronize()
-    graph = torch.cuda.CUDAGraph()
-    c0 = B.ha_launch_count()
-    with torch.cuda.graph(graph, stream=stream):
-        step()
-    launches_per_step = B.ha_launch_count() - c0
-    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    graphs = {}
+    for marks in (False, True):
+        g = torch.cuda.CUDAGraph()
+        c0 = B.ha_launch_count()
+        with torch.cuda.graph(g, stream=stream):
+            step(marks)
+        graphs[marks] = g
+        launches_per_step = B.ha_launch_count() - c0
+    graph = graphs[False]
+    # L2 flush before every timed step: write 256 MiB, then read another 256 MiB, so
+    # that neither our data nor dirty lines of the write are left in L2 (a write-
+    # only flush leaves 126 MB of dirty lines whose write-back would share DRAM
+    # with the timed step)
+    flush_w = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    flush_r = torch.ones(64 << 20, dtype=torch.float32, device=dev)
+    flush_out = torch.empty((), dtype=torch.float32, device=dev)
 
-    def timed(k):
+    def flush(i):
+        flush_w.fill_(i & 0xFF)
+        torch.sum(flush_r, dim=0, out=flush_out)
+
+    def timed(g, k):
         per = [[0.0] * (n_ev - 1) for _ in range(k)]
         tot = []
         for i in range(k):
-            flush.fill_(i & 0xFF)
-            graph.replay()
+            flush(i)
+            g.replay()
             torch.cuda.synchronize()
-            for j in range(n_ev - 1):
-                per[i][j] = ev[j].elapsed_time(ev[j + 1])
+            if g is graphs[True]:
+                for j in range(n_ev - 1):
+                    per[i][j] = ev[j].elapsed_time(ev[j + 1])
             tot.append(ev[0].elapsed_time(ev[n_ev - 1]))
         return tot, per
 
     for _ in range(args.warmup):
+        flush(0)
         graph.replay()
+        graphs[True].replay()
     torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
     with ClockSampler(dev) as clocks:
         t_wall0 = time.perf_counter()
-        tot, per = timed(args.steps)
+        tot, _ = timed(graph, args.steps)
         torch.cuda.synchronize()
         t_wall = time.perf_counter() - t_wall0
     if world > 1:
@@ -385,6 +411,8 @@ def main():
     total_ms = float(t_max.item())
     tokens = w.B * world * args.steps
     value = tokens / (total_ms / 1e3)
+    # per-kernel breakdown: the same steps with an event between every two calls
+    tot_marked, per = timed(graphs[True], args.steps)
     kern_ms = {n: sum(p[j] for p in per) / len(per) for j, n in enumerate(names)}
 
     # ---- roofline of the dominant kernel (largest share of the step)
@@ -423,7 +451,7 @@ def main():
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e2e_ms = []
     for i in range(args.steps):
-        flush.fill_(i & 0xFF)
+        flush(i)
         torch.cuda.synchronize()
         with torch.cuda.stream(stream):
             e0.record(stream)
@@ -461,8 +489,8 @@ def main():
                    "n_win": w.n_win, "m": w.m, "k": w.k if w.kind == "csa" else None,
                    "H_I": w.H_I if w.kind == "csa" else None,
                    "d_I": w.d_I if w.kind == "csa" else None,
-                   "l2": "flushed (256 MiB write) before every timed step",
-                   "timing": "CUDA events inside a CUDA graph, per step"},
+                   "l2": "flushed before every timed step (256 MiB write, then 256 MiB read)",
+                   "timing": "CUDA events at both ends of a CUDA graph of the step, per step"},
         "clocks": clk,
         "e2e": {"value": round(e2e_value, 1), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
@@ -470,6 +498,7 @@ def main():
         "roofline": roofline,
         "cpu_baseline": cpu,
         "kernel_ms": {k: round(v, 5) for k, v in kern_ms.items()},
+        "ms_per_step_with_kernel_events": round(sum(tot_marked) / len(tot_marked), 5),
         "step_algorithmic_gbs": round(sum(nbytes.values()) / (step_ms * 1e-3) / 1e9, 1),
         "wall_s_timed": round(t_wall, 3),
     }

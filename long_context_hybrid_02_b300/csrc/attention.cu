@@ -43,6 +43,7 @@ struct AttnArgs {
 
 template <typename T, int DPL>
 __global__ void __launch_bounds__(kThreads) attn_simt(AttnArgs a) {
+  pdl_wait_then_release();
   constexpr int V = Elem<T>::kVec;
   extern __shared__ __align__(16) unsigned char smem_raw[];
   const int row = blockIdx.x;
@@ -195,6 +196,7 @@ __global__ void __launch_bounds__(128) attn_merge(const float* __restrict__ o_pa
                                                   float* __restrict__ lse) {
   extern __shared__ float wts[];                  // [S]
   __shared__ float s_inv;
+  pdl_wait_then_release();
   const int row = blockIdx.x, h = blockIdx.y;
   const float* lp = lse_part + (long long)row * S * H + h;
   if (threadIdx.x < 32) {
@@ -252,8 +254,7 @@ cudaError_t launch_dpl(const AttnArgs& a, int rows, size_t smem, cudaStream_t st
   cudaError_t e = ensure_smem(reinterpret_cast<const void*>(kern), smem);
   if (e != cudaSuccess) return e;
   const dim3 grid(rows, a.n_splits, (a.H + kHeadsPerCta - 1) / kHeadsPerCta);
-  kern<<<grid, kThreads, smem, st>>>(a);
-  return launched(cudaGetLastError());
+  return launch_pdl(kern, grid, dim3(kThreads), smem, st, 1, a);
 }
 
 template <typename T>
@@ -270,9 +271,8 @@ cudaError_t launch_t(const AttnArgs& a, int rows, cudaStream_t st) {
     default: e = launch_dpl<T, 32>(a, rows, smem, st); break;
   }
   if (e != cudaSuccess || a.n_splits == 1) return e;
-  attn_merge<T><<<dim3(rows, a.H), 128, a.n_splits * sizeof(float), st>>>(
-      a.o_part, a.lse_part, a.n_splits, a.H, a.d, static_cast<T*>(a.o), a.lse);
-  return launched(cudaGetLastError());
+  return launch_pdl(attn_merge<T>, dim3(rows, a.H), dim3(128), a.n_splits * sizeof(float), st, 1,
+                    a.o_part, a.lse_part, a.n_splits, a.H, a.d, static_cast<T*>(a.o), a.lse);
 }
 
 }  // namespace
@@ -280,12 +280,10 @@ cudaError_t launch_t(const AttnArgs& a, int rows, cudaStream_t st) {
 cudaError_t launch_attn_merge(const ha_params& p, int rows, int S, const float* o_part,
                               const float* lse_part, void* o, float* lse, cudaStream_t st) {
   if (p.dtype == HA_BF16)
-    attn_merge<__nv_bfloat16><<<dim3(rows, p.H), 128, S * sizeof(float), st>>>(
-        o_part, lse_part, S, p.H, p.d, static_cast<__nv_bfloat16*>(o), lse);
-  else
-    attn_merge<float><<<dim3(rows, p.H), 128, S * sizeof(float), st>>>(
-        o_part, lse_part, S, p.H, p.d, static_cast<float*>(o), lse);
-  return launched(cudaGetLastError());
+    return launch_pdl(attn_merge<__nv_bfloat16>, dim3(rows, p.H), dim3(128), S * sizeof(float), st,
+                      1, o_part, lse_part, S, p.H, p.d, static_cast<__nv_bfloat16*>(o), lse);
+  return launch_pdl(attn_merge<float>, dim3(rows, p.H), dim3(128), S * sizeof(float), st, 1,
+                    o_part, lse_part, S, p.H, p.d, static_cast<float*>(o), lse);
 }
 
 AttnPlan plan_attention_simt(const ha_params& p, int rows, int max_keys, bool decode) {

@@ -239,6 +239,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_decode_tc(const TcArgs a) {
   __syncthreads();
   tc::fence_after_sync();
   const uint32_t tmem = *tmem_slot;
+  pdl_wait_then_release();                  // the set-up above touched no global memory
 
   if (warp < 4) {
     // ------------------------------------------------------------------ producer
@@ -731,23 +732,10 @@ cudaError_t launch_attention_tc(const ha_params& p, const AttnPlan& pl, int deco
   (void)ws;
   cudaError_t e = ensure_smem(reinterpret_cast<const void*>(attn_decode_tc), kSmem);
   if (e != cudaSuccess) return e;
-  cudaLaunchConfig_t cfg = {};
-  cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = kSmem;
-  cfg.stream = st;
-  cudaLaunchAttribute attr[1];
-  if (a.cluster_merge) {
-    cfg.gridDim = dim3(unsigned(a.n_items));               // one item per CTA
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = unsigned(a.S);
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-  } else {
-    cfg.gridDim = dim3(unsigned(a.n_items < num_sms() ? a.n_items : num_sms()));
-  }
-  return launched(cudaLaunchKernelEx(&cfg, attn_decode_tc, a));
+  const long long grid = a.cluster_merge ? a.n_items                    // one item per CTA
+                                         : (a.n_items < num_sms() ? a.n_items : num_sms());
+  return launch_pdl(attn_decode_tc, dim3(unsigned(grid)), dim3(kThreads), kSmem, st,
+                    a.cluster_merge ? unsigned(a.S) : 1u, a);
 }
 
 }  // namespace ha

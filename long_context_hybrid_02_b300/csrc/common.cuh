@@ -17,6 +17,45 @@ cudaError_t ensure_smem(const void* func, size_t bytes);
 // Count one successful kernel launch (ha_launch_count) and pass the status on.
 cudaError_t launched(cudaError_t e);
 
+// Launch `kernel` on `st` as a programmatic dependent of the stream's previous
+// kernel: it may be scheduled while that kernel is still running, and must call
+// pdl_wait() before it reads or writes any global memory.  cluster_x > 1 also
+// groups the CTAs into thread-block clusters of cluster_x CTAs.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t st, unsigned cluster_x, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[2];
+  unsigned n = 0;
+  attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[n].val.programmaticStreamSerializationAllowed = 1;
+  ++n;
+  if (cluster_x > 1) {
+    attr[n].id = cudaLaunchAttributeClusterDimension;
+    attr[n].val.clusterDim.x = cluster_x;
+    attr[n].val.clusterDim.y = 1;
+    attr[n].val.clusterDim.z = 1;
+    ++n;
+  }
+  cfg.attrs = attr;
+  cfg.numAttrs = n;
+  return launched(cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...));
+}
+
+// Wait until the preceding kernel of the stream has completed and its memory is
+// visible (a no-op when the kernel was not launched as a programmatic dependent);
+// then let the next kernel of the stream be scheduled.  Every kernel calls this
+// before its first global-memory access, so any kernel launched after it sees
+// every earlier kernel complete.
+__device__ __forceinline__ void pdl_wait_then_release() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ---------------------------------------------------------------- storage types
 template <typename T> struct Elem;
 template <> struct Elem<float> {

@@ -39,6 +39,7 @@ __device__ __forceinline__ void locate(const CompressArgs& a, int c, int& tsr, i
 template <typename T>
 __global__ void __launch_bounds__(256) compress_small_m(CompressArgs a) {
   constexpr int V = Elem<T>::kVec;
+  pdl_wait_then_release();
   const int total_chunks = a.chunks[0] + a.chunks[1] + a.chunks[2];
   const long long n_items = (long long)a.B * a.n_blk * total_chunks;
   for (long long it = blockIdx.x * (long long)blockDim.x + threadIdx.x; it < n_items;
@@ -104,6 +105,7 @@ __host__ __device__ inline int n_groups(int m) {
 template <typename T>
 __global__ void __launch_bounds__(512) compress_large_m(CompressArgs a) {
   constexpr int V = Elem<T>::kVec;
+  pdl_wait_then_release();
   extern __shared__ float sm[];                    // alpha[m] | partial[G][kSlice][V]
   const int G = n_groups(a.m);
   const int per_group = (a.m + G - 1) / G;
@@ -193,17 +195,15 @@ cudaError_t launch(const CompressArgs& a, cudaStream_t st) {
     const long long n_items = (long long)a.B * a.n_blk * total_chunks;
     const long long want = (n_items + 255) / 256;
     const int grid = int(want < 148LL * 32 ? want : 148LL * 32);
-    compress_small_m<T><<<grid, 256, 0, st>>>(a);
-    return launched(cudaGetLastError());
+    return launch_pdl(compress_small_m<T>, dim3(grid), dim3(256), 0, st, 1, a);
   } else {
     const int G = n_groups(a.m);
     const dim3 grid(a.B * a.n_blk, (total_chunks + kSlice - 1) / kSlice);
     const size_t smem = (size_t(((a.m + 3) & ~3)) + size_t(G) * kSlice * Elem<T>::kVec) * sizeof(float);
     cudaError_t e = ensure_smem(reinterpret_cast<const void*>(compress_large_m<T>), smem);
     if (e != cudaSuccess) return e;
-    compress_large_m<T><<<grid, G * kSlice, smem, st>>>(a);
+    return launch_pdl(compress_large_m<T>, grid, dim3(G * kSlice), smem, st, 1, a);
   }
-  return launched(cudaGetLastError());
 }
 
 }  // namespace

@@ -21,6 +21,7 @@ __global__ void __launch_bounds__(256) index_scores_simt(const T* __restrict__ q
                                                          int m, int elig,
                                                          float* __restrict__ scores) {
   constexpr int V = Elem<T>::kVec;
+  pdl_wait_then_release();
   extern __shared__ float sq[];                    // q [H_I][d_I] | w [H_I]
   float* sw = sq + H_I * d_I;
   const int row = blockIdx.x;                      // b * Tq + t
@@ -62,18 +63,17 @@ cudaError_t launch_index_scores_simt(const ha_params& p, const void* q_idx, cons
     auto k = index_scores_simt<__nv_bfloat16>;
     cudaError_t e = ensure_smem(reinterpret_cast<const void*>(k), smem);
     if (e != cudaSuccess) return e;
-    k<<<grid, 256, smem, st>>>(static_cast<const __nv_bfloat16*>(q_idx), w_idx,
-                               static_cast<const __nv_bfloat16*>(cki), n_cap, q_pos, Tq, p.H_I,
-                               p.d_I, p.n_win, p.m, p.elig, scores);
+    return launch_pdl(k, grid, dim3(256), smem, st, 1, static_cast<const __nv_bfloat16*>(q_idx),
+                      w_idx, static_cast<const __nv_bfloat16*>(cki), n_cap, q_pos, Tq, p.H_I,
+                      p.d_I, p.n_win, p.m, p.elig, scores);
   } else {
     auto k = index_scores_simt<float>;
     cudaError_t e = ensure_smem(reinterpret_cast<const void*>(k), smem);
     if (e != cudaSuccess) return e;
-    k<<<grid, 256, smem, st>>>(static_cast<const float*>(q_idx), w_idx,
-                               static_cast<const float*>(cki), n_cap, q_pos, Tq, p.H_I, p.d_I,
-                               p.n_win, p.m, p.elig, scores);
+    return launch_pdl(k, grid, dim3(256), smem, st, 1, static_cast<const float*>(q_idx), w_idx,
+                      static_cast<const float*>(cki), n_cap, q_pos, Tq, p.H_I, p.d_I, p.n_win,
+                      p.m, p.elig, scores);
   }
-  return launched(cudaGetLastError());
 }
 
 }  // namespace ha

@@ -128,6 +128,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     index_scores_tc(const __grid_constant__ CUtensorMap map_k,
                     const __grid_constant__ CUtensorMap map_q, IdxArgs a) {
   using C = Cfg<QT>;
+  pdl_wait_then_release();
   extern __shared__ unsigned char smem_raw[];
   unsigned char* base = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -292,8 +293,8 @@ cudaError_t launch_qt(const ha_params& p, const void* q_idx, const float* w_idx,
     if (e != cudaSuccess) return e;
   }
   IdxArgs a{w_idx, q_pos, scores, p.B, Tq, n_cap, p.n_win, p.m, p.elig, err};
-  index_scores_tc<QT><<<g_num_sms, kThreads, C::kSmem, st>>>(map_k, map_q, a);
-  return launched(cudaGetLastError());
+  return launch_pdl(index_scores_tc<QT>, dim3(g_num_sms), dim3(kThreads), C::kSmem, st, 1, map_k,
+                    map_q, a);
 }
 
 }  // namespace

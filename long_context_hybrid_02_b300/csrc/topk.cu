@@ -80,6 +80,7 @@ __global__ void __launch_bounds__(kThreads) topk_cluster(const float* __restrict
                                                          int seg_len, int32_t* __restrict__ idx) {
   extern __shared__ uint32_t skeys[];
   __shared__ TopkShared sh;
+  pdl_wait_then_release();
   cg::cluster_group cluster = cg::this_cluster();
   const int C = int(cluster.num_blocks());
   const int rank = int(cluster.block_rank());
@@ -233,21 +234,8 @@ cudaError_t launch_topk(const ha_params& p, const float* scores, int n_cap, cons
   const size_t smem = size_t(seg_len < kSmemKeys ? seg_len : kSmemKeys) * sizeof(uint32_t);
   cudaError_t e = ensure_smem(reinterpret_cast<const void*>(topk_cluster), smem);
   if (e != cudaSuccess) return e;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(unsigned(rows * C));
-  cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = st;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = unsigned(C);
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  e = cudaLaunchKernelEx(&cfg, topk_cluster, scores, n_cap, q_pos, p.k, p.n_win, p.m, p.elig,
-                         seg_len, idx);
-  return launched(e);
+  return launch_pdl(topk_cluster, dim3(unsigned(rows * C)), dim3(kThreads), smem, st, unsigned(C),
+                    scores, n_cap, q_pos, p.k, p.n_win, p.m, p.elig, seg_len, idx);
 }
 
 }  // namespace ha
