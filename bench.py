@@ -254,16 +254,26 @@ def run_reference(args, rank):
     w = synth.WORKLOADS[args.workload]
     tok, qry = host_inputs(w, 1)
     per_step = max(0.5, min(5.0, 120.0 / max(1, args.steps + args.warmup)))
+
+    def one(seconds):
+        if w.decode:
+            d, e, th, _ = oracle_sample(w, tok, qry, 1, seconds)
+        else:
+            d, e, th = oracle_prefill_sample(w, tok, qry, seconds)
+        return d, e, th
+
     for _ in range(args.warmup):
-        oracle_sample(w, tok, qry, 1, 0.0)
+        one(0.0)
     done, el = 0, 0.0
     for _ in range(args.steps):
-        d, e, threads, _ = oracle_sample(w, tok, qry, 1, per_step)
+        d, e, threads = one(per_step)
         done += d
         el += e
     value = done / el
     cores = len(os.sched_getaffinity(0))
-    line = {"impl": "reference", "metric": "decode tokens/s (one layer, all sequences)",
+    metric = ("decode tokens/s (one layer, all sequences)" if w.decode
+              else "prefill tokens/s (one layer, one chunk)")
+    line = {"impl": "reference", "metric": metric,
             "value": value, "unit": "tokens/s", "n_gpus": args.gpus, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": 1e3 * el / max(1, done),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
@@ -277,6 +287,193 @@ def run_reference(args, rank):
             "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
+
+
+# ----------------------------------------------------------------------------- prefill
+def oracle_prefill_sample(w, tok_h, qry_h, seconds: float):
+    """The oracle's prefill of sequence 0, one query after the other from the end of
+    the chunk, until `seconds` pass.  Returns (queries done, wall seconds, threads)."""
+    import numpy as np
+    import oracle as O
+
+    def f64(t):
+        return t.to("cpu").float().numpy().astype(np.float64)
+
+    g = tok_h["gate"][0].numpy().astype(np.float64)
+    K, V = f64(tok_h["k_tok"][0]), f64(tok_h["v_tok"][0])
+    ck = O.compress(K, g, w.m, 0, w.n_blocks, w.dtype)
+    cv = O.compress(V, g, w.m, 0, w.n_blocks, w.dtype)
+    cki = O.compress(f64(tok_h["ki_tok"][0]), g, w.m, 0, w.n_blocks, w.dtype)
+    done, t0 = 0, time.perf_counter()
+    while True:
+        i = w.Tq - 1 - (done % w.Tq)
+        t = w.L - w.Tq + i
+        ne = O.n_eligible(t, w.n_win, w.m)
+        sc = O.index_scores(f64(qry_h["qI"][0, i]), f64(qry_h["w_idx"][0, i]), cki[:ne])
+        idx = O.topk_select(sc, w.k)
+        O.prefill_query(f64(qry_h["q"][0, i]), idx, ck, cv, K, V, t, n_win=w.n_win, m=w.m,
+                        scale=1 / math.sqrt(w.d))
+        done += 1
+        if time.perf_counter() - t0 >= seconds:
+            break
+    return done, time.perf_counter() - t0, blas_threads()
+
+
+def run_prefill(args, w, dev, world, rank, dist):
+    """One prefill chunk of Tq queries per sequence: index every eligible entry for
+    every query (tensor-core GEMM), top-k per query, attention per query over its
+    selection and causal window."""
+    import torch
+    from long_context_hybrid_02_b300 import binding as B
+    from long_context_hybrid_02_b300 import synth
+    from long_context_hybrid_02_b300.pipeline import HybridLayer
+    tok = synth.make_tokens(w, dev)
+    qry = synth.make_queries(w, dev)
+    layer = HybridLayer(w, tok, dev)
+    layer.build_cache()
+    stream = torch.cuda.Stream(device=dev)
+    names = ["index", "topk", "attention"]
+    ev = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(4)]
+    ws = (layer.ws.data_ptr(), layer.ws.numel())
+
+    def step(marks: bool):
+        s = stream.cuda_stream
+        ev[0].record(stream)
+        B.csa_index_scores(layer.p, qry["qI"], qry["w_idx"], layer.cki, layer.n_cap, qry["q_pos"],
+                           w.Tq, layer.scores, s)
+        if marks:
+            ev[1].record(stream)
+        B.csa_topk(layer.p, layer.scores, layer.n_cap, qry["q_pos"], w.Tq, layer.idx, ws, s)
+        if marks:
+            ev[2].record(stream)
+        B.hybrid_attn_prefill(layer.p, qry["q"], qry["q_pos"], w.Tq, layer.ck, layer.cv,
+                              layer.n_cap, layer.idx, tok["k_tok"], tok["v_tok"], layer.tok_cap,
+                              layer.o, layer.lse, ws, s)
+        ev[3].record(stream)
+
+    with torch.cuda.stream(stream):
+        step(True)
+    torch.cuda.synchronize()
+    graphs = {}
+    for marks in (False, True):
+        g = torch.cuda.CUDAGraph()
+        c0 = B.ha_launch_count()
+        with torch.cuda.graph(g, stream=stream):
+            step(marks)
+        graphs[marks] = g
+        launches_per_step = B.ha_launch_count() - c0
+    flush_w = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    flush_r = torch.ones(64 << 20, dtype=torch.float32, device=dev)
+    flush_out = torch.empty((), dtype=torch.float32, device=dev)
+
+    def timed(g, k):
+        tot, per = [], []
+        for i in range(k):
+            flush_w.fill_(i & 0xFF)
+            torch.sum(flush_r, dim=0, out=flush_out)
+            g.replay()
+            torch.cuda.synchronize()
+            tot.append(ev[0].elapsed_time(ev[3]))
+            if g is graphs[True]:
+                per.append([ev[j].elapsed_time(ev[j + 1]) for j in range(3)])
+        return tot, per
+
+    for _ in range(args.warmup):
+        graphs[False].replay()
+        graphs[True].replay()
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    with ClockSampler(dev) as clocks:
+        t_wall0 = time.perf_counter()
+        tot, _ = timed(graphs[False], args.steps)
+        t_wall = time.perf_counter() - t_wall0
+    if world > 1:
+        dist.barrier()
+    t_max = torch.tensor([sum(tot)], dtype=torch.float64, device=dev)
+    if world > 1:
+        dist.all_reduce(t_max, op=dist.ReduceOp.MAX)
+    tokens = w.B * w.Tq * world * args.steps
+    value = tokens / (float(t_max.item()) / 1e3)
+    step_ms = sum(tot) / len(tot)
+    tot_marked, per = timed(graphs[True], args.steps)
+    kern_ms = {n: sum(p[j] for p in per) / len(per) for j, n in enumerate(names)}
+
+    # algorithmic flops: attention 4*H*d per (query, key); indexer 2*H_I*d_I per (query, entry)
+    pos = qry["q_pos"].to("cpu").long()
+    t = pos.reshape(-1)
+    ne = torch.clamp(t + 1 - w.n_win, min=0) // w.m
+    keys = torch.clamp(ne, max=w.k) + torch.clamp(t + 1, max=w.n_win)
+    attn_flops = float(4 * w.H * w.d * keys.sum().item())
+    idx_flops = float(2 * w.H_I * w.d_I * ne.sum().item())
+    pk = peaks()
+    att_tf = attn_flops / (kern_ms["attention"] * 1e-3) / 1e12
+    idx_tf = idx_flops / (kern_ms["index"] * 1e-3) / 1e12
+    roofline = {"bound": "tensor", "kernel": "attention", "achieved": round(att_tf, 1),
+                "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
+                "frac": round(att_tf / pk["bf16_tflops"], 4), "traffic": None,
+                "algorithmic_flops": attn_flops,
+                "peak_source": pk["source"] + " (MEASURED_PEAKS.json bf16_tflops, burst)"}
+
+    # end to end: the chunk's queries from pinned host memory, outputs back
+    h_in = {k: torch.empty_like(qry[k], device="cpu").pin_memory() for k in ("q", "qI", "w_idx")}
+    for k in h_in:
+        h_in[k].copy_(qry[k])
+    h_out = torch.empty_like(layer.o, device="cpu").pin_memory()
+    h2d = sum(x.numel() * x.element_size() for x in h_in.values())
+    d2h = h_out.numel() * h_out.element_size()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e2e_ms = []
+    for i in range(args.steps):
+        flush_w.fill_(i & 0xFF)
+        torch.sum(flush_r, dim=0, out=flush_out)
+        torch.cuda.synchronize()
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            for k in h_in:
+                qry[k].copy_(h_in[k], non_blocking=True)
+            graphs[False].replay()
+            h_out.copy_(layer.o, non_blocking=True)
+            e1.record(stream)
+        e1.synchronize()
+        e2e_ms.append(e0.elapsed_time(e1))
+    e2e_value = w.B * w.Tq * world * args.steps / (sum(e2e_ms) / 1e3)
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        tok_h = {k: v[:1].to("cpu") for k, v in tok.items()}
+        qry_h = {k: v[:1].to("cpu") for k, v in qry.items()}
+        done, el, threads = oracle_prefill_sample(w, tok_h, qry_h, args.cpu_seconds)
+        cpu = {"value": done / el, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+               "host_cpus": len(os.sched_getaffinity(0)),
+               "sample": f"{done} prefill queries of sequence 0 (from the end of the chunk), "
+                         f"{el:.1f}s; caches built untimed"}
+    line = {
+        "metric": "prefill tokens/s (one layer, one chunk)",
+        "value": round(value, 1), "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(step_ms, 5), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded Gaussian drawn on the device)",
+        "config": {"workload": w.name, "kind": w.kind, "B": w.B, "ctx": w.L, "Tq": w.Tq, "H": w.H,
+                   "d": w.d, "n_win": w.n_win, "m": w.m, "k": w.k, "H_I": w.H_I, "d_I": w.d_I,
+                   "l2": "flushed before every timed step (256 MiB write, then 256 MiB read)",
+                   "timing": "CUDA events at both ends of a CUDA graph of the step, per step"},
+        "clocks": clocks.summary(),
+        "e2e": {"value": round(e2e_value, 1), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": int(launches_per_step) * args.steps,
+        "roofline": roofline,
+        "indexer_tflops": round(idx_tf, 1),
+        "cpu_baseline": cpu,
+        "kernel_ms": {k: round(v, 5) for k, v in kern_ms.items()},
+        "ms_per_step_with_kernel_events": round(sum(tot_marked) / len(tot_marked), 5),
+        "wall_s_timed": round(t_wall, 3),
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
 
 
 # ----------------------------------------------------------------------------- GPU arm
@@ -310,9 +507,12 @@ def main():
         w = w.scaled(B=args.batch)
     if args.ctx > 0:
         w = w.scaled(L=args.ctx)
-    assert w.decode, "the benchmark times decode workloads"
+    if not w.decode:
+        return run_prefill(args, w, dev, world, rank, dist)
     tok = synth.make_tokens(w, dev)
     qry = synth.make_queries(w, dev)
+    if w.plant_frac > 0:
+        synth.plant_blocks(w, tok, qry, max(0, w.L - w.n_win) // w.m)
     layer = HybridLayer(w, tok, dev)
     layer.build_cache()
     new_blk = torch.full((w.B,), (w.L // w.m) - 1 if w.L % w.m == 0 else -1, dtype=torch.int32,

@@ -23,9 +23,13 @@ std::mutex g_grant_mu;
 }  // namespace
 
 cudaError_t ensure_smem(const void* func, size_t bytes) {
-  if (bytes <= 48 * 1024) return cudaSuccess;
+  // the default limit (48 KiB) covers static plus dynamic shared memory together
+  cudaFuncAttributes fa;
+  cudaError_t e = cudaFuncGetAttributes(&fa, func);
+  if (e != cudaSuccess) return e;
+  if (bytes + fa.sharedSizeBytes <= 48 * 1024) return cudaSuccess;
   int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
+  e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   std::lock_guard<std::mutex> lock(g_grant_mu);
   for (int i = 0; i < g_n_grants; ++i)

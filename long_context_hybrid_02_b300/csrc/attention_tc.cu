@@ -67,7 +67,8 @@ constexpr int kTmemCols = 512;
 constexpr int kSCol = 0;                         // two S buffers: columns [0, 128)
 constexpr int kOCol = 2 * kHG;                   // O^T: 4 x 64 columns [128, 384)
 constexpr int kTokFlag = 1 << 30;                // slot code: per-token row
-constexpr int kMaxClusterSplits = 8;             // splits merged inside the kernel
+constexpr int kMaxClusterSplits = 16;            // splits the in-kernel merge supports
+constexpr int kPreferredClusterSplits = 8;       // splits the launch plan uses at most
 constexpr float kRescaleLog2 = 8.f;              // P <= 2^8 before the reference moves
 
 constexpr size_t kSmemRing = size_t(kRing) * kStageBytes;
@@ -75,9 +76,15 @@ constexpr size_t kSmemTbl = size_t(4) * 2 * kTile * 4;           // [warp][tile 
 constexpr size_t kSmemMisc = (4 * 64 + 64 + 64 + 2 * 64) * 4 + 32 * 8 + 16;
 constexpr size_t kSmem = 1024 + kQBytes + kSmemRing + kPBytes + kSmemTbl + kSmemMisc;
 static_assert(kSmem <= 232448, "shared-memory budget");
-// receive buffer of the in-cluster merge: [8 splits][64 heads][64 dims] .. [3][64][172]
-static_assert(3 * 64 * 172 * 4 <= kSmemRing + kPBytes && 7 * 64 * 76 * 4 <= kSmemRing + kPBytes,
-              "merge buffer");
+// receive buffer of the in-cluster merge, [S][64 heads][W] float32 with W the slice
+// width rounded up to 4, must fit the ring + P (contiguous) for every S
+constexpr bool merge_buffer_fits() {
+  for (int S = 2; S <= kMaxClusterSplits; ++S)
+    if (size_t(S) * 64 * (((kD + S - 1) / S + 3) / 4 * 4) * 4 > kSmemRing + kPBytes) return false;
+  return true;
+}
+static_assert(merge_buffer_fits(), "merge buffer");
+static_assert(kMaxClusterSplits * 64 * 4 <= 4 * 2 * kTile * 4, "lse buffer (row tables)");
 
 struct TcArgs {
   const bf16* q;         // [rows, H, 512]
@@ -582,9 +589,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_decode_tc(const TcArgs a) {
     const Item x = item_of(a, blockIdx.x);
     const int S = a.S, me = x.split;
     const int W = ((kD + S - 1) / S + 3) / 4 * 4;            // row width of the receive buffer
-    float* recv = reinterpret_cast<float*>(ring);             // [S][64 heads][W]
-    float* lse_in = reinterpret_cast<float*>(tbl_all);        // [S][64]
-    float* wts = lse_in + kMaxClusterSplits * kHG;            // [S][64]
+    float* recv = reinterpret_cast<float*>(ring);             // [S][64 heads][W] (ring + P)
+    float* lse_in = reinterpret_cast<float*>(tbl_all);        // [S][64] (the row tables)
+    float* wts = reinterpret_cast<float*>(sQ);                // [S][64] (q is idle now)
+    float* inv = wts + kMaxClusterSplits * kHG;               // [64]
     cluster.sync();
     if (warp >= 5) {
       const int sw = warp - 5, quarter = warp & 3, row = quarter * 32 + lane;
@@ -612,7 +620,6 @@ __global__ void __launch_bounds__(kThreads, 1) attn_decode_tc(const TcArgs a) {
       }
     }
     cluster.sync();                                           // every piece has arrived
-    float* inv = stats;                                       // [64]
     const int h0 = x.hg * kHG;
     if (threadIdx.x < kHG) {
       const int h = threadIdx.x;
@@ -676,13 +683,47 @@ bool attention_tc_supported(const ha_params& p, int n_cap, int tok_cap) {
          (long long)p.B * n_cap < kTokFlag && (long long)p.B * tok_cap < kTokFlag;
 }
 
+// Largest cluster (number of splits merged in the kernel) the current device can
+// schedule with this kernel's resources: 16 needs the non-portable cluster size.
+int max_cluster_splits() {
+  static int cached[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 8;
+  if (cached[dev] != 0) return cached[dev];
+  int best = 8;
+  if (ensure_smem(reinterpret_cast<const void*>(attn_decode_tc), kSmem) == cudaSuccess &&
+      cudaFuncSetAttribute(reinterpret_cast<const void*>(attn_decode_tc),
+                           cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(kMaxClusterSplits);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = kSmem;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = kMaxClusterSplits;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, attn_decode_tc, &cfg) == cudaSuccess && n > 0)
+      best = kMaxClusterSplits;
+  }
+  (void)cudaGetLastError();
+  cached[dev] = best;
+  return best;
+}
+
 AttnPlan plan_attention_tc(const ha_params& p, int rows, int max_keys) {
   AttnPlan pl{};
   const long long units = (long long)rows * (p.H / kHG);
   const int sms = num_sms();
   // enough splits to cover the SMs, at most what one cluster merges
+  // (8 = the portable cluster size: clusters of 16 need a whole GPC each and fewer of
+  // them are resident at a time, which measured slower on B300)
   int S = units >= sms ? 1 : int(sms / units);
-  if (S > kMaxClusterSplits) S = kMaxClusterSplits;
+  if (S > kPreferredClusterSplits) S = kPreferredClusterSplits;
+  if (S > max_cluster_splits()) S = max_cluster_splits();
   if (S < 1) S = 1;
   int kps = (max_keys + S - 1) / S;
   kps = (kps + 15) / 16 * 16;

@@ -3,8 +3,8 @@
 //
 // Exact radix select over order-preserving 32-bit keys of the float scores (NaN
 // ranks as -inf).  A row is handled by a thread-block cluster of C CTAs (C = 1
-// when there are enough rows to fill the GPU); CTA r of the cluster holds the
-// keys of segment r of the row in shared memory.
+// when there are enough rows to fill the GPU, up to 16 for a few long rows); CTA
+// r of the cluster holds the keys of segment r of the row in shared memory.
 //   1. three passes over 11-, 11- and 10-bit digits, most significant first: every
 //      CTA histograms the keys of its segment that still match the selected prefix
 //      (warp-aggregated shared-memory atomics), the C histograms are summed over
@@ -32,7 +32,7 @@ namespace {
 constexpr int kThreads = 512;
 constexpr int kWarps = kThreads / 32;
 constexpr int kBins = 2048;
-constexpr int kMaxCluster = 8;
+constexpr int kMaxCluster = 16;
 constexpr int kSmemKeys = 40 * 1024;      // keys held in shared memory per CTA
 
 struct TopkShared {
@@ -218,6 +218,38 @@ int num_sms() {
   return g_num_sms[dev];
 }
 
+// Largest cluster the current device can schedule for this kernel with a full
+// shared-memory segment: 16 needs the non-portable cluster size, else 8.
+int max_cluster() {
+  static int cached[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 8;
+  if (cached[dev] != 0) return cached[dev];
+  int best = 8;
+  const size_t smem = size_t(kSmemKeys) * sizeof(uint32_t);
+  if (ensure_smem(reinterpret_cast<const void*>(topk_cluster), smem) == cudaSuccess &&
+      cudaFuncSetAttribute(reinterpret_cast<const void*>(topk_cluster),
+                           cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(kMaxCluster);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = kMaxCluster;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, topk_cluster, &cfg) == cudaSuccess && n > 0)
+      best = kMaxCluster;
+  }
+  (void)cudaGetLastError();
+  cached[dev] = best;
+  return best;
+}
+
 }  // namespace
 
 size_t topk_workspace_bytes(const ha_params&, int, int) { return 0; }
@@ -227,9 +259,10 @@ cudaError_t launch_topk(const ha_params& p, const float* scores, int n_cap, cons
   const long long rows = (long long)p.B * Tq;
   // CTAs per row: enough to cover the GPU when rows are few, and enough for every
   // segment to fit the shared-memory budget when possible.
+  const int c_max = max_cluster();
   int C = 1;
-  while (C < kMaxCluster && rows * C < num_sms()) C *= 2;
-  while (C < kMaxCluster && (n_cap + C - 1) / C > kSmemKeys) C *= 2;
+  while (C < c_max && rows * C < num_sms()) C *= 2;
+  while (C < c_max && (n_cap + C - 1) / C > kSmemKeys) C *= 2;
   const int seg_len = (n_cap + C - 1) / C;
   const size_t smem = size_t(seg_len < kSmemKeys ? seg_len : kSmemKeys) * sizeof(uint32_t);
   cudaError_t e = ensure_smem(reinterpret_cast<const void*>(topk_cluster), smem);

@@ -103,3 +103,14 @@ def test_topk_signed_zeros_tie():
     idx = _run(s, q_pos, k)
     _check(s, q_pos, idx, k)
     assert idx[0, 0].tolist() == list(range(k))
+
+
+@pytest.mark.parametrize("rows,n_cap", [(148, 10000), (80, 16384), (300, 9000)])
+def test_topk_segments_near_the_default_shared_memory_limit(rows, n_cap):
+    """Segments whose keys (plus the kernel's static shared memory) pass the 48 KiB
+    default, with and without clusters."""
+    k = 512
+    s = _scores((1, rows, n_cap), 20 + rows, ties=8)
+    q_pos = torch.full((1, rows), 128 + 4 * n_cap - 1, dtype=torch.int32)
+    idx = _run(s, q_pos, k)
+    _check(s, q_pos, idx, k)
