@@ -110,13 +110,15 @@ def compress(X, gate, m: int, j_begin: int, n_blk: int, storage: str | None = No
     """
     X = np.asarray(X)
     gate = np.asarray(gate)
-    out = np.empty((n_blk, X.shape[1]), dtype=np.float64)
-    for b in range(n_blk):
-        j = j_begin + b
-        lo, hi = j * m, (j + 1) * m
-        if hi > X.shape[0]:
-            raise ValueError(f"block {j} is not complete")
-        out[b] = compress_block(X[lo:hi], gate[lo:hi])
+    lo, hi = j_begin * m, (j_begin + n_blk) * m
+    if hi > X.shape[0]:
+        raise ValueError(f"block {j_begin + n_blk - 1} is not complete")
+    # every block at once: the same per-block softmax-gated sum as compress_block
+    g = np.asarray(gate[lo:hi], dtype=np.float64).reshape(n_blk, m)
+    e = np.exp(g - g.max(axis=1, keepdims=True))
+    alpha = e / e.sum(axis=1, keepdims=True)                      # [n_blk, m]
+    rows = np.asarray(X[lo:hi], dtype=np.float64).reshape(n_blk, m, X.shape[1])
+    out = np.einsum("bi,bid->bd", alpha, rows)
     return out if storage is None else round_to_storage(out, storage)
 
 
