@@ -621,8 +621,8 @@ def main():
     dom = max(kern_ms, key=kern_ms.get)
     pk = peaks()
     achieved = nbytes[dom] / (kern_ms[dom] * 1e-3) / 1e9
-    src_of = {"compress": "compress.cu", "index": "indexer.cu", "topk": "topk.cu",
-              "attention": "attention.cu"}
+    src_of = {"compress": "compress.cu", "index": "indexer_tc.cu", "topk": "topk.cu",
+              "attention": "attention_tc.cu"}
     traffic = profiled_traffic(dom, src_of[dom])
     roofline = {"bound": "hbm", "kernel": dom, "achieved": round(achieved, 1),
                 "peak": pk["hbm_gbs"], "unit": "GB/s", "frac": round(achieved / pk["hbm_gbs"], 4),

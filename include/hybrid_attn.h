@@ -163,7 +163,9 @@ ha_status csa_topk(const ha_params* p, const float* scores, int32_t n_cap,
  *   o          : T [B, H, d]           lse : float [B, H] or NULL
  *   ws         : ha_workspace_size(p, HA_OP_DECODE, 1, n_cap) bytes (split
  *                partials: the key list is split across CTAs and merged in a
- *                fixed order).
+ *                fixed order).  0 bytes (ws may be NULL) for bfloat16, d = 512
+ *                and H a multiple of 64, where the splits of a sequence merge
+ *                inside the kernel.
  * ------------------------------------------------------------------------- */
 ha_status hybrid_attn_decode(const ha_params* p, const void* q, const void* ck, const void* cv,
                              int32_t n_cap, const int32_t* idx, const void* k_tok,
