@@ -5,8 +5,9 @@ Default workload: CSA decode, 32 sequences at 65,536 tokens, 64 query heads of
 dim 512 on one shared K/V head, window 128, m = 4 (16,384 entries per
 sequence), top-512, indexer 64 heads x 128, bfloat16 storage, fp32 accumulation.
 One step = one decode token per sequence through the whole path: compress the
-block completed by the newest token, score every eligible entry, select the
-top-k, attend to selection + window (split-KV + merge).  The step's launches are
+block completed by the newest token (on a side stream: under the disjoint
+eligibility rule that block is not visible to the step's own query), score every
+eligible entry, select the top-k, attend to selection + window.  The step's launches are
 captured once in a CUDA graph and replayed; timing uses CUDA events recorded at
 both ends of the graph on the launching stream, with an L2 flush (256 MiB write,
 then 256 MiB read) before every timed step.  The library's kernels are chained
@@ -153,18 +154,22 @@ def peaks():
             "source": "fallback"}
 
 
-def profiled_traffic(kernel_name: str, source_file: str):
-    """DRAM bytes per launch of `kernel_name` from the committed ncu summary, or None
-    when there is none or the kernel's source changed since the capture."""
+def profiled_traffic(workload: str | None, kernel_name: str, source_file: str):
+    """DRAM bytes per launch of `kernel_name` in `workload` from the committed ncu
+    summary, or None when there is none or the kernel's source changed since the
+    capture."""
+    if workload is None:
+        return None
     path = os.path.join(ROOT, "profiles", "dram_traffic.md")
     if not os.path.exists(path):
         return None
     src = os.path.join(ROOT, "long_context_hybrid_02_b300", "csrc", source_file)
     sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
     for line in open(path):
-        m = re.match(r"\|\s*(\S+)\s*\|\s*(\S+)\s*\|\s*([0-9.eE+]+)\s*\|\s*([0-9a-f]{16})\s*\|", line)
-        if m and m.group(1) == kernel_name and m.group(4) == sha:
-            return float(m.group(3))
+        m = re.match(r"\|\s*(\S+)\s*\|\s*(\S+)\s*\|\s*(\S+)\s*\|\s*([0-9.eE+]+)\s*\|"
+                     r"\s*([0-9a-f]{16})\s*\|", line)
+        if m and m.group(1) == workload and m.group(2) == kernel_name and m.group(5) == sha:
+            return float(m.group(4))
     return None
 
 
@@ -523,14 +528,29 @@ def main():
     n_ev = len(names) + 1
     ev = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(n_ev)]
 
+    side = torch.cuda.Stream(device=dev)
+    fork, join = torch.cuda.Event(), torch.cuda.Event()
+    # Under the disjoint rule with n_win >= m the newest complete block lies inside
+    # the query's window and is not eligible, so its compression can run beside
+    # index / top-k / attention.
+    concurrent_compress = layer.p.elig == B.ELIG_DISJOINT and w.n_win >= w.m
+
     def step(marks: bool):
         """One decode step.  The first and last events are always recorded; with
         marks, also one between every two calls (the per-kernel breakdown: a
         recorded event between two kernels also keeps the second from starting
-        early, so the headline graph has none)."""
+        early, so the headline graph has none), and the calls run one after the
+        other; without, the compression runs on a side stream."""
         s = stream.cuda_stream
         ev[0].record(stream)
-        layer.compress(new_blk, 1, s)
+        overlap = concurrent_compress and not marks
+        if not overlap:
+            layer.compress(new_blk, 1, s)
+        else:
+            fork.record(stream)
+            side.wait_event(fork)
+            layer.compress(new_blk, 1, side.cuda_stream)
+            join.record(side)
         if marks:
             ev[1].record(stream)
         if w.kind == "csa":
@@ -548,11 +568,14 @@ def main():
         B.hybrid_attn_decode(layer.p, q, layer.ck, layer.cv, layer.n_cap, idx, tok["k_tok"],
                              tok["v_tok"], layer.tok_cap, qry["ctx_len"], layer.o, layer.lse,
                              (layer.ws.data_ptr(), layer.ws.numel()), s)
+        if overlap:
+            stream.wait_event(join)
         ev[n_ev - 1].record(stream)
 
     # eager warm-up (sets kernel attributes), then capture both graphs
     with torch.cuda.stream(stream):
         step(True)
+        step(False)
     torch.cuda.synchronize()
     graphs = {}
     for marks in (False, True):
@@ -623,7 +646,8 @@ def main():
     achieved = nbytes[dom] / (kern_ms[dom] * 1e-3) / 1e9
     src_of = {"compress": "compress.cu", "index": "indexer_tc.cu", "topk": "topk.cu",
               "attention": "attention_tc.cu"}
-    traffic = profiled_traffic(dom, src_of[dom])
+    full_size = args.ctx == 0 and args.batch == 0
+    traffic = profiled_traffic(args.workload if full_size else None, dom, src_of[dom])
     roofline = {"bound": "hbm", "kernel": dom, "achieved": round(achieved, 1),
                 "peak": pk["hbm_gbs"], "unit": "GB/s", "frac": round(achieved / pk["hbm_gbs"], 4),
                 "traffic": traffic, "algorithmic_bytes": nbytes[dom],

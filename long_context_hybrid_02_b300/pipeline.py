@@ -47,6 +47,10 @@ class HybridLayer:
             nb = max(nb, B.ha_workspace_size(self.p, B.OP_TOPK, Tq, self.n_cap, True))
         self.ws = torch.empty((max(nb, 16),), dtype=torch.uint8, device=device)
         self.blk_zero = torch.zeros((w.B,), dtype=torch.int32, device=device)
+        # side stream for the decode step's compression (see decode_step)
+        self._side = torch.cuda.Stream(device=device)
+        self._fork = torch.cuda.Event()
+        self._join = torch.cuda.Event()
 
     # ------------------------------------------------------------------ caches
     def compress(self, blk_begin: torch.Tensor, n_blk: int, stream=None):
@@ -68,9 +72,25 @@ class HybridLayer:
 
         new_blk: int32 [B] index of the block completed by the newest token, or None
         when no block completed at this step.  q_pos = ctx_len - 1 (int32 [B, 1]).
+
+        Under the disjoint eligibility rule a block is visible to a query only once it
+        ends before the query's window.  The newest complete block ends at most m - 1
+        tokens before the query, so with n_win >= m it is not visible to this step:
+        its compression then runs on a side stream beside scoring, selection and
+        attention, and the step's stream waits for it before returning.  Otherwise
+        (overlap rule, or n_win < m) the block is compressed first.
         """
+        main = torch.cuda.ExternalStream(B._stream(stream))
+        joined = False
         if new_blk is not None:
-            self.compress(new_blk, 1, stream)
+            if self.p.elig == B.ELIG_DISJOINT and self.p.n_win >= self.p.m:
+                self._fork.record(main)
+                self._side.wait_event(self._fork)
+                self.compress(new_blk, 1, self._side.cuda_stream)
+                self._join.record(self._side)
+                joined = True
+            else:
+                self.compress(new_blk, 1, stream)
         ws = (self.ws.data_ptr(), self.ws.numel())
         if self.csa:
             B.csa_index_scores(self.p, qI, w_idx, self.cki, self.n_cap, q_pos, 1, self.scores, stream)
@@ -82,6 +102,8 @@ class HybridLayer:
             B.hybrid_attn_decode(self.p, q, self.ck, self.cv, self.n_cap, None, self.tok["k_tok"],
                                  self.tok["v_tok"], self.tok_cap, ctx_len, self.o, self.lse, ws,
                                  stream)
+        if joined:
+            main.wait_event(self._join)
         return self.o
 
     def prefill_chunk(self, q, q_pos, qI=None, w_idx=None, stream=None):

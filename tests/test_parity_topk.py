@@ -1,11 +1,12 @@
 """csa_topk against the oracle's selection, bit-exact, in every launch configuration.
 
-The kernel splits a row over a cluster of up to 8 CTAs when rows are few, keeps
-each CTA's segment in shared memory up to 40,960 keys and re-reads longer
-segments from global memory, and uses one CTA per row when rows are many.  The
-scores are fed identically to both sides (float32), so the index sets must be
-identical: ties broken by the smaller index, NaN ranked as -inf, output in
-ascending index order with -1 padding.
+Rows of up to 40,960 entries go to one 1024-thread CTA each (keys in shared
+memory, early stop of the digit passes, bitmap-ordered write).  Longer rows are
+split over a cluster of up to 16 CTAs, each holding its segment in shared memory
+up to 40,960 keys and re-reading longer segments from global memory.  The scores
+are fed identically to both sides (float32), so the index sets must be identical:
+ties broken by the smaller index, NaN ranked as -inf, output in ascending index
+order with -1 padding.
 """
 import numpy as np
 import pytest
@@ -112,5 +113,62 @@ def test_topk_segments_near_the_default_shared_memory_limit(rows, n_cap):
     k = 512
     s = _scores((1, rows, n_cap), 20 + rows, ties=8)
     q_pos = torch.full((1, rows), 128 + 4 * n_cap - 1, dtype=torch.int32)
+    idx = _run(s, q_pos, k)
+    _check(s, q_pos, idx, k)
+
+
+@pytest.mark.parametrize("n_cap", [40960, 40961])
+def test_topk_largest_one_cta_row_and_first_cluster_row(n_cap):
+    """The last row length held by one CTA, and the first one split over a cluster."""
+    k = 1024
+    s = _scores((3, 1, n_cap), 30, ties=64, nans=200)
+    q_pos = torch.full((3, 1), 128 + 4 * n_cap - 1, dtype=torch.int32)
+    q_pos[2, 0] = 128 + 4 * (n_cap - 37) - 1                # ragged: not a multiple of 32
+    idx = _run(s, q_pos, k)
+    _check(s, q_pos, idx, k)
+
+
+def test_topk_one_cta_all_equal_and_threshold_ties():
+    """Every digit pass runs to the end: the whole row, or a large share of it, ties
+    at the threshold, and the ties are taken by index."""
+    n_cap, k = 20000, 512
+    s = torch.full((4, 1, n_cap), 0.25)
+    s[1, 0, 5000:5100] = 3.0                                 # 100 above, the rest tied
+    s[2, 0, ::3] = float("nan")                              # NaN below every tie
+    s[3, 0, 19000:] = torch.arange(1000, dtype=torch.float32) # distinct top, ties below
+    q_pos = torch.full((4, 1), 128 + 4 * n_cap - 1, dtype=torch.int32)
+    idx = _run(s, q_pos, k)
+    _check(s, q_pos, idx, k)
+    assert idx[0, 0].tolist() == list(range(k))
+
+
+def test_topk_one_cta_bin_taken_whole():
+    """The k largest keys sit alone in the top first-digit bins: the passes stop
+    after the first one."""
+    n_cap, k = 9000, 512
+    g = torch.Generator().manual_seed(31)
+    s = torch.rand((2, 1, n_cap), generator=g)               # [0, 1)
+    pick = torch.randperm(n_cap, generator=g)[:k]
+    s[0, 0, pick] = 1e6                                      # one bin holds exactly k keys
+    s[1, 0, pick] = 1e6 + torch.arange(k, dtype=torch.float32) * 64
+    q_pos = torch.full((2, 1), 128 + 4 * n_cap - 1, dtype=torch.int32)
+    idx = _run(s, q_pos, k)
+    _check(s, q_pos, idx, k)
+    assert sorted(pick.tolist()) == idx[0, 0].tolist()
+
+
+def test_topk_one_cta_sample_blind_rows():
+    """Rows whose large scores sit where the strided threshold sample never looks
+    (period 16 at phase 3), and rows of fewer than 4,096 keys that all tie: the
+    kernel's sampled threshold misjudges them and the exact passes over every key
+    take over."""
+    n_cap, k = 16384, 512
+    g = torch.Generator().manual_seed(32)
+    s = torch.rand((3, 1, n_cap), generator=g)
+    s[0, 0, 3::16] += 5.0                                    # 1,024 large keys, unseen by the sample
+    s[1, 0, 3::16] += torch.rand(1024, generator=g) * 5.0
+    s[2, 0, :] = 1.0
+    q_pos = torch.full((3, 1), 128 + 4 * n_cap - 1, dtype=torch.int32)
+    q_pos[2, 0] = 128 + 4 * 3000 - 1                         # 3,000 tied keys
     idx = _run(s, q_pos, k)
     _check(s, q_pos, idx, k)
