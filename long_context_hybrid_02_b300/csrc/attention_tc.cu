@@ -29,7 +29,8 @@
 //              of each tile, K one tile ahead of V, with 16-byte cp.async into a
 //              ring of kRing 32 KiB stages (warp w fills every stage g with
 //              g % kRing == w and blocks only on its own copies; empty slots are
-//              zero-filled);
+//              zero-filled; a tile of R <= 32 or <= 64 used rows takes R/32
+//              stages per operand, each holding R rows x 16384/R dims);
 //   warp 4     MMA issuer (one thread): S(t+1) into the second score buffer while
 //              the softmax works on S(t), then P(t).V(t);
 //   warps 5-8  softmax of each tile (TMEM lane = key), O^T rescaling, and at the
@@ -129,6 +130,14 @@ __device__ __forceinline__ Item item_of(const TcArgs& a, long long it) {
   const int n = x.hi - x.lo;
   x.nt = n > 0 ? (n + kTile - 1) / kTile : 1;
   return x;
+}
+
+// Key rows a tile's stages hold: the tile's slots rounded up to 32, 64 or 128.  A
+// 32 KiB stage holds R rows x 16384/R dims (256/R swizzled 64-dim halves of R x
+// 128 B), so a tile takes R/32 stages for K and as many for V.
+__device__ __forceinline__ int tile_rows(const Item& x, int t) {
+  const int n = x.hi - x.lo - t * kTile;
+  return n <= 32 ? 32 : (n <= 64 ? 64 : kTile);
 }
 
 // Entry named by compressed slot `slot` (< n_c): idx[r, slot] (CSA) or slot (HCA).
@@ -281,6 +290,37 @@ __global__ void __launch_bounds__(kThreads, 1) attn_decode_tc(const TcArgs a) {
       const Item x = item_of(a, it);
       // stages: K(0); then per tile t: K(t+1), V(t).  A warp touches every tile (each
       // run of 4 stages holds one of its stages) and keeps that tile's row table.
+      // stage j of a tile with R rows: rows 0..R-1, 64-dim halves [j*hbs, (j+1)*hbs)
+      auto fill = [&](int t, const bf16* comp, const bf16* tok, int err_code) -> bool {
+        const int* tbl = tbl_all + (w * 2 + (t & 1)) * kTile;
+        const int R = tile_rows(x, t), hbs = 256 / R;
+        for (int j = 0; j < R / 32; ++j, ++g) {
+          if (int(g % kRing) != w) continue;
+          if (!tc::mbar_wait(&empty[w], uint32_t(((g / kRing) & 1) ^ 1), a.err, err_code)) return false;
+          // 8 rows at a time: their codes in registers first (the copies are asm
+          // statements with a memory clobber; table reads between them would be
+          // serialised), then the copies of every half
+#pragma unroll 1
+          for (int i0 = 0; i0 < R / 4; i0 += 8) {
+            int cd[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) cd[u] = tbl[rsub + 4 * (i0 + u)];
+#pragma unroll 1
+            for (int hb = 0; hb < hbs; ++hb) {
+              const int col = (j * hbs + hb) * 64 + ch * 8;
+              const uint32_t half_base = stage + hb * (R * 128);
+#pragma unroll
+              for (int u = 0; u < 8; ++u) {
+                const int row = rsub + 4 * (i0 + u);
+                put(half_base + row * 128 + ((ch ^ (row & 7)) << 4), cd[u], comp, tok, col);
+              }
+            }
+          }
+          publish(&full[w]);
+        }
+        return true;
+      };
+      // K stages of tile t: the warp's copy of the tile's row table first
       auto k_stages = [&](int t) -> bool {
         int* tbl = tbl_all + (w * 2 + (t & 1)) * kTile;
         __syncwarp();
@@ -291,54 +331,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_decode_tc(const TcArgs a) {
         for (int j = 0; j < kTile / 32; ++j)
           tbl[lane + 32 * j] = slot_code(a, x, x.lo + t * kTile + lane + 32 * j, ent[j]);
         __syncwarp();
-        for (int pair = 0; pair < 4; ++pair, ++g) {
-          if (int(g % kRing) != w) continue;
-          if (!tc::mbar_wait(&empty[w], uint32_t(((g / kRing) & 1) ^ 1), a.err, 41)) return false;
-          // 8 rows at a time: their codes in registers first (the copies are asm
-          // statements with a memory clobber; table reads between them would be
-          // serialised), then 16 copies
-#pragma unroll 1
-          for (int i0 = 0; i0 < kTile / 4; i0 += 8) {
-            int cd[8];
-#pragma unroll
-            for (int u = 0; u < 8; ++u) cd[u] = tbl[rsub + 4 * (i0 + u)];
-#pragma unroll
-            for (int hb = 0; hb < 2; ++hb) {
-              const int kb = 2 * pair + hb;
-#pragma unroll
-              for (int u = 0; u < 8; ++u) {
-                const int row = rsub + 4 * (i0 + u);
-                put(stage + hb * kHalfBytes + row * 128 + ((ch ^ (row & 7)) << 4), cd[u], a.ck,
-                    a.k_tok, kb * 64 + ch * 8);
-              }
-            }
-          }
-          publish(&full[w]);
-        }
-        return true;
+        return fill(t, a.ck, a.k_tok, 41);
       };
-      auto v_stages = [&](int t) -> bool {
-        const int* tbl = tbl_all + (w * 2 + (t & 1)) * kTile;
-        for (int mb = 0; mb < kD / 128; ++mb, ++g) {
-          if (int(g % kRing) != w) continue;
-          if (!tc::mbar_wait(&empty[w], uint32_t(((g / kRing) & 1) ^ 1), a.err, 42)) return false;
-#pragma unroll 1
-          for (int i0 = 0; i0 < kTile / 4; i0 += 8) {
-            int cd[8];
-#pragma unroll
-            for (int u = 0; u < 8; ++u) cd[u] = tbl[rsub + 4 * (i0 + u)];
-#pragma unroll
-            for (int u = 0; u < 8; ++u) {
-              const int row = rsub + 4 * (i0 + u);
-              const uint32_t off = row * 128 + ((ch ^ (row & 7)) << 4);
-              put(stage + off, cd[u], a.cv, a.v_tok, mb * 128 + ch * 8);
-              put(stage + kHalfBytes + off, cd[u], a.cv, a.v_tok, mb * 128 + 64 + ch * 8);
-            }
-          }
-          publish(&full[w]);
-        }
-        return true;
-      };
+      auto v_stages = [&](int t) -> bool { return fill(t, a.cv, a.v_tok, 42); };
       // q of the item: every warp copies a quarter, once the previous item's score
       // MMAs are done with the buffer; its copies stay in flight (their own group)
       // while the first tile's table is built, and are published before the first
@@ -359,6 +354,15 @@ __global__ void __launch_bounds__(kThreads, 1) attn_decode_tc(const TcArgs a) {
         if (t + 1 < x.nt && !(ok = k_stages(t + 1))) break;
         ok = v_stages(t);
       }
+      // an item of fewer than kRing stages leaves some warps without a stage of
+      // their own: they publish their quarter of q here (no wait of theirs depends
+      // on this item's MMAs, so this cannot hold up the score MMA)
+      if (ok && q_pending) {
+        tc::cp_async_wait<0>();
+        tc::fence_proxy_async_smem();
+        tc::mbar_arrive(q_full);
+        q_pending = false;
+      }
     }
     tc::cp_async_wait<0>();
   } else if (warp == 4) {
@@ -369,26 +373,27 @@ __global__ void __launch_bounds__(kThreads, 1) attn_decode_tc(const TcArgs a) {
       const uint32_t q_base = tc::smem_u32(sQ), p_base = tc::smem_u32(sP);
       long long g = 0, n = 0, G = 0;   // stage, item and global tile counters
       bool ok = true;
-      // S(tile Gt) from its 4 K stages into score buffer Gt & 1
-      auto s_mma = [&](long long Gt) -> bool {
-        const int buf = int(Gt & 1);
+      // S(tile Gt, R key rows) from its R/32 K stages into score buffer Gt & 1.  The
+      // MMA reads 128 rows from each half; rows R..127 belong to the next half or
+      // stage (any values): their scores are never used.
+      auto s_mma = [&](long long Gt, int R) -> bool {
+        const int buf = int(Gt & 1), hbs = 256 / R;
         if (!tc::mbar_wait(&s_empty[buf], uint32_t(((Gt >> 1) & 1) ^ 1), a.err, 43)) return false;
         tc::fence_after_sync();
-        for (int pair = 0; pair < 4; ++pair, ++g) {
+        for (int j = 0; j < R / 32; ++j, ++g) {
           const int s = int(g % kRing);
           if (!tc::mbar_wait(&full[s], uint32_t((g / kRing) & 1), a.err, 44)) return false;
           tc::fence_after_sync();
           const uint32_t sa = tc::smem_u32(ring + size_t(s) * kStageBytes);
+          for (int hb = 0; hb < hbs; ++hb) {
+            const int kb = j * hbs + hb;
 #pragma unroll
-          for (int hb = 0; hb < 2; ++hb)
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk) {
-              const int kb = 2 * pair + hb;
+            for (int kk = 0; kk < 4; ++kk)
               tc::mma_bf16(tmem + kSCol + buf * kHG,
-                           tc::sdesc_kmajor_sw128(sa + hb * kHalfBytes + kk * 32),
+                           tc::sdesc_kmajor_sw128(sa + hb * (R * 128) + kk * 32),
                            tc::sdesc_kmajor_sw128(q_base + kb * (kHG * 128) + kk * 32), idesc_s,
                            (kb | kk) != 0 ? 1u : 0u);
-            }
+          }
           tc::mma_commit(&empty[s]);
         }
         tc::mma_commit(&s_full[buf]);
@@ -398,27 +403,32 @@ __global__ void __launch_bounds__(kThreads, 1) attn_decode_tc(const TcArgs a) {
         const Item x = item_of(a, it);
         if (!(ok = tc::mbar_wait(q_full, uint32_t(n & 1), a.err, 45))) break;
         tc::fence_after_sync();
-        if (!(ok = s_mma(G))) break;
+        if (!(ok = s_mma(G, tile_rows(x, 0)))) break;
         if (x.nt == 1) tc::mma_commit(q_empty);
         for (int t = 0; t < x.nt && ok; ++t, ++G) {
           if (t + 1 < x.nt) {
-            if (!(ok = s_mma(G + 1))) break;
+            if (!(ok = s_mma(G + 1, tile_rows(x, t + 1)))) break;
             if (t + 2 == x.nt) tc::mma_commit(q_empty);
           }
           if (!(ok = tc::mbar_wait(p_full, uint32_t(G & 1), a.err, 46))) break;
           if (t == 0 && !(ok = tc::mbar_wait(o_empty, uint32_t((n & 1) ^ 1), a.err, 47))) break;
           tc::fence_after_sync();
-          for (int mb = 0; mb < kD / 128 && ok; ++mb, ++g) {
+          // V stage j holds dims [64*j*hbs, 64*(j+1)*hbs) of the tile's R keys, i.e.
+          // the 128-dim O^T blocks j*hbs/2 .. (j+1)*hbs/2 - 1; R/16 K steps per block
+          const int R = tile_rows(x, t), hbs = 256 / R;
+          for (int j = 0; j < R / 32 && ok; ++j, ++g) {
             const int s = int(g % kRing);
             if (!(ok = tc::mbar_wait(&full[s], uint32_t((g / kRing) & 1), a.err, 48))) break;
             tc::fence_after_sync();
             const uint32_t sa = tc::smem_u32(ring + size_t(s) * kStageBytes);
-#pragma unroll
-            for (int kk = 0; kk < kTile / 16; ++kk)
-              tc::mma_bf16(tmem + kOCol + mb * kHG,
-                           tc::sdesc_sw128(sa + kk * 2048, kHalfBytes, 1024),
-                           tc::sdesc_sw128(p_base + kk * 2048, kHalfBytes, 1024), idesc_o,
-                           (t | kk) != 0 ? 1u : 0u);
+            for (int mbl = 0; mbl < hbs / 2; ++mbl) {
+              const int mb = j * (hbs / 2) + mbl;
+              for (int kk = 0; kk < R / 16; ++kk)
+                tc::mma_bf16(tmem + kOCol + mb * kHG,
+                             tc::sdesc_sw128(sa + 2 * mbl * (R * 128) + kk * 2048, R * 128, 1024),
+                             tc::sdesc_sw128(p_base + kk * 2048, kHalfBytes, 1024), idesc_o,
+                             (t | kk) != 0 ? 1u : 0u);
+            }
             tc::mma_commit(&empty[s]);
           }
           if (ok) tc::mma_commit(pv_done);
@@ -582,8 +592,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_decode_tc(const TcArgs a) {
     // CTA r owns the head dims [lo(r), lo(r + 1)), lo(r) = 4 * floor(128 r / S).
     // After a first barrier (every CTA's ring is idle), each CTA sends its
     // normalised o, dim by dim, to the owner of the dim and its lse to everyone,
-    // with remote shared-memory stores; after a second barrier each CTA merges
-    // its dims in split order:
+    // with remote shared-memory stores (one head per store: the 32 lanes hold 32
+    // consecutive dims, so each store is one 128-byte segment; 16-byte stores of
+    // 4 heads per lane scatter a warp's store over 32 segments and were slower);
+    // after a second barrier each CTA merges its dims in split order:
     //   o = sum_s exp(lse_s - mx) o_s / sum_s exp(lse_s - mx),  lse = mx + log(sum).
     cg::cluster_group cluster = cg::this_cluster();
     const Item x = item_of(a, blockIdx.x);

@@ -220,3 +220,24 @@ def test_tc_decode_hca_long_rows_need_more_than_eight_splits():
         ro, rl = O.attend(np64(q[b]), keys, vals, 1 / math.sqrt(D))
         assert_close(np64(o[b]), ro, "bf16", f"o[{b}]")
         assert_close(np64(lse[b]), rl, "bf16", f"lse[{b}]")
+
+
+@pytest.mark.parametrize("Bn,k", [(48, 512), (32, 512), (20, 512), (32, 200)])
+def test_tc_decode_split_tails_of_every_size(Bn, k):
+    """Batch sizes that give 3, 4 and 7 splits per row: the last tile of a split
+    holds 128, 96, 64, 40 or 32 keys, so every compact tail size (32, 64 and 128
+    rows per stage set) meets real keys."""
+    L, m, n_win = 4096, 4, 128
+    n_cap = L // m
+    k_tok, v_tok, ck, cv = _caches(Bn, L, n_cap, 400 + Bn + k)
+    q = synth.gaussian((Bn, 64, D), DEV, 410 + Bn, 1 / math.sqrt(D), torch.bfloat16)
+    ne = O.n_eligible(L - 1, n_win, m)
+    idx = synth.random_index_sets(Bn, 1, k, torch.full((Bn, 1), ne), "cpu", 9)[:, 0].clone()
+    p = B.make_params(Bn, 64, D, n_win, m, k, 1, 8, B.BF16)
+    ctx_t = torch.full((Bn,), L, dtype=torch.int32, device=DEV)
+    o, lse = _decode(p, q, ck, cv, n_cap, idx.to(DEV), k_tok, v_tok, L, ctx_t)
+    CK, CV = np64(ck), np64(cv)
+    for b in range(Bn):
+        sel = [int(j) for j in idx[b]]
+        _check_row(o[b], lse[b], np64(q[b]), sel, CK[b], CV[b], np64(k_tok[b]), np64(v_tok[b]),
+                   L - 1, n_win, 1 / math.sqrt(D), f"seq {b}")
