@@ -36,10 +36,10 @@
 //   warps 5-8  softmax of each tile (TMEM lane = key), O^T rescaling, and at the
 //              end of the item the epilogue (TMEM lane = head dim).
 // Rows with one split: persistent grid (one CTA per SM) looping over items.  Rows
-// with 2..8 splits: one item per CTA and the splits of a row form a thread-block
-// cluster; every CTA sends each head dim of its normalised o to the CTA that owns
-// that dim with remote shared-memory stores, and every CTA merges its dims (no
-// workspace, no second launch).
+// with 2..16 splits: one item per CTA and the splits of a row form a thread-block
+// cluster; every CTA stages its normalised o in its own shared memory and merges
+// the head dims it owns by reading every split's o from its peers' shared memory
+// (no workspace, no second launch).
 // Every wait is bounded (tc::kWaitLimitNs); on timeout the kernel records an error
 // code in the library's device error word and returns.
 #include <cooperative_groups.h>
@@ -77,15 +77,10 @@ constexpr size_t kSmemTbl = size_t(4) * 2 * kTile * 4;           // [warp][tile 
 constexpr size_t kSmemMisc = (4 * 64 + 64 + 64 + 2 * 64) * 4 + 32 * 8 + 16;
 constexpr size_t kSmem = 1024 + kQBytes + kSmemRing + kPBytes + kSmemTbl + kSmemMisc;
 static_assert(kSmem <= 232448, "shared-memory budget");
-// receive buffer of the in-cluster merge, [S][64 heads][W] float32 with W the slice
-// width rounded up to 4, must fit the ring + P (contiguous) for every S
-constexpr bool merge_buffer_fits() {
-  for (int S = 2; S <= kMaxClusterSplits; ++S)
-    if (size_t(S) * 64 * (((kD + S - 1) / S + 3) / 4 * 4) * 4 > kSmemRing + kPBytes) return false;
-  return true;
-}
-static_assert(merge_buffer_fits(), "merge buffer");
-static_assert(kMaxClusterSplits * 64 * 4 <= 4 * 2 * kTile * 4, "lse buffer (row tables)");
+// the in-cluster merge stages o as float32 [64][512] over the ring and keeps its
+// weights [S][64] and 1/sum [64] in q's space
+static_assert(size_t(kHG) * kD * 4 <= kSmemRing, "merge staging");
+static_assert((kMaxClusterSplits + 1) * kHG * 4 <= kQBytes, "merge weights");
 
 struct TcArgs {
   const bf16* q;         // [rows, H, 512]
@@ -114,21 +109,32 @@ struct Item {
   int nt;         // tiles (>= 1 even when the range is empty)
 };
 
-__device__ __forceinline__ Item item_of(const TcArgs& a, long long it) {
+// The fields of item `it` that need no global read (row, head group, split, lo).
+__device__ __forceinline__ Item item_head(const TcArgs& a, long long it) {
   Item x;
   x.split = int(it % a.S);
   const long long rest = it / a.S;
   x.hg = int(rest % a.HG);
   x.r = int(rest / a.HG);
   x.b = x.r / a.Tq;
+  x.lo = x.split * a.kps;
+  return x;
+}
+
+// The rest, from the query position.
+__device__ __forceinline__ void item_tail(const TcArgs& a, Item& x) {
   x.t = a.decode ? a.pos[x.b] - 1 : a.pos[x.r];
   x.ne = x.t >= 0 ? n_eligible(x.t, a.n_win, a.m, a.elig, a.n_cap) : 0;
   x.n_c = a.idx ? a.k : x.ne;
   x.n_w = x.t >= 0 ? min(a.n_win, x.t + 1) : 0;
-  x.lo = x.split * a.kps;
   x.hi = min(x.n_c + x.n_w, x.lo + a.kps);
   const int n = x.hi - x.lo;
   x.nt = n > 0 ? (n + kTile - 1) / kTile : 1;
+}
+
+__device__ __forceinline__ Item item_of(const TcArgs& a, long long it) {
+  Item x = item_head(a, it);
+  item_tail(a, x);
   return x;
 }
 
@@ -287,9 +293,29 @@ __global__ void __launch_bounds__(kThreads, 1) attn_decode_tc(const TcArgs a) {
       tc::mbar_arrive(bar);
     };
     for (long long it = blockIdx.x; it < a.n_items && ok; it += gridDim.x, ++n) {
-      const Item x = item_of(a, it);
-      // stages: K(0); then per tile t: K(t+1), V(t).  A warp touches every tile (each
-      // run of 4 stages holds one of its stages) and keeps that tile's row table.
+      // q of the item: every warp copies a quarter, once the previous item's score
+      // MMAs are done with the buffer; its copies stay in flight (their own group)
+      // while the first tile's table is built, and are published with this warp's
+      // first stage.  q and the first tile's entries need no query position, so
+      // they are requested before it is read.
+      Item x = item_head(a, it);
+      if (!(ok = tc::mbar_wait(q_empty, uint32_t((n & 1) ^ 1), a.err, 40))) break;
+      const bf16* qrow = a.q + ((long long)x.r * a.H + x.hg * kHG) * kD;
+#pragma unroll
+      for (int i = 0; i < kQBytes / 16 / 128; ++i) {   // 32 chunks per thread
+        const int c = pt + 128 * i;
+        const int kb = c >> 9, h = (c >> 3) & 63;
+        tc::cp_async16(q_base + kb * (kHG * 128) + h * 128 + ((ch ^ (h & 7)) << 4),
+                       qrow + (long long)h * kD + kb * 64 + ch * 8);
+      }
+      tc::cp_async_commit();
+      q_pending = true;
+      int ent0[kTile / 32];
+#pragma unroll
+      for (int j = 0; j < kTile / 32; ++j) ent0[j] = slot_entry(a, x, x.lo + lane + 32 * j);
+      item_tail(a, x);
+      // stages: K(0); then per tile t: K(t+1), V(t).  Every warp keeps its own copy
+      // of the row table of the tiles in flight, whether or not it fills a stage.
       // stage j of a tile with R rows: rows 0..R-1, 64-dim halves [j*hbs, (j+1)*hbs)
       auto fill = [&](int t, const bf16* comp, const bf16* tok, int err_code) -> bool {
         const int* tbl = tbl_all + (w * 2 + (t & 1)) * kTile;
@@ -326,7 +352,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_decode_tc(const TcArgs a) {
         __syncwarp();
         int ent[kTile / 32];
 #pragma unroll
-        for (int j = 0; j < kTile / 32; ++j) ent[j] = slot_entry(a, x, x.lo + t * kTile + lane + 32 * j);
+        for (int j = 0; j < kTile / 32; ++j)
+          ent[j] = t == 0 ? ent0[j] : slot_entry(a, x, x.lo + t * kTile + lane + 32 * j);
 #pragma unroll
         for (int j = 0; j < kTile / 32; ++j)
           tbl[lane + 32 * j] = slot_code(a, x, x.lo + t * kTile + lane + 32 * j, ent[j]);
@@ -334,21 +361,6 @@ __global__ void __launch_bounds__(kThreads, 1) attn_decode_tc(const TcArgs a) {
         return fill(t, a.ck, a.k_tok, 41);
       };
       auto v_stages = [&](int t) -> bool { return fill(t, a.cv, a.v_tok, 42); };
-      // q of the item: every warp copies a quarter, once the previous item's score
-      // MMAs are done with the buffer; its copies stay in flight (their own group)
-      // while the first tile's table is built, and are published before the first
-      // stage of this warp
-      if (!(ok = tc::mbar_wait(q_empty, uint32_t((n & 1) ^ 1), a.err, 40))) break;
-      const bf16* qrow = a.q + ((long long)x.r * a.H + x.hg * kHG) * kD;
-#pragma unroll
-      for (int i = 0; i < kQBytes / 16 / 128; ++i) {   // 32 chunks per thread
-        const int c = pt + 128 * i;
-        const int kb = c >> 9, h = (c >> 3) & 63;
-        tc::cp_async16(q_base + kb * (kHG * 128) + h * 128 + ((ch ^ (h & 7)) << 4),
-                       qrow + (long long)h * kD + kb * 64 + ch * 8);
-      }
-      tc::cp_async_commit();
-      q_pending = true;
       if (!(ok = k_stages(0))) break;
       for (int t = 0; t < x.nt && ok; ++t) {
         if (t + 1 < x.nt && !(ok = k_stages(t + 1))) break;
@@ -589,59 +601,60 @@ __global__ void __launch_bounds__(kThreads, 1) attn_decode_tc(const TcArgs a) {
   __syncthreads();
   if (a.cluster_merge) {
     // Every CTA of the cluster holds one split of the same query row and head group.
-    // CTA r owns the head dims [lo(r), lo(r + 1)), lo(r) = 4 * floor(128 r / S).
-    // After a first barrier (every CTA's ring is idle), each CTA sends its
-    // normalised o, dim by dim, to the owner of the dim and its lse to everyone,
-    // with remote shared-memory stores (one head per store: the 32 lanes hold 32
-    // consecutive dims, so each store is one 128-byte segment; 16-byte stores of
-    // 4 heads per lane scatter a warp's store over 32 segments and were slower);
-    // after a second barrier each CTA merges its dims in split order:
+    // Each CTA stages its normalised o as float32 [64 heads][512 dims] over its idle
+    // ring, with the eight warps that can read its tensor memory (warps 0-3 and 5-8;
+    // lanes = consecutive dims, so every store is one 128-byte row segment).  After
+    // a cluster barrier, CTA r merges the dims [lo(r), lo(r + 1)), lo(r) =
+    // 4 floor(128 r / S), reading every split's o and lse from the peers' shared
+    // memory (16-byte loads, 512 contiguous bytes per warp), in split order:
     //   o = sum_s exp(lse_s - mx) o_s / sum_s exp(lse_s - mx),  lse = mx + log(sum).
+    // A last barrier keeps every CTA's shared memory alive until its peers are done.
+    tc::fence_after_sync();
     cg::cluster_group cluster = cg::this_cluster();
     const Item x = item_of(a, blockIdx.x);
     const int S = a.S, me = x.split;
-    const int W = ((kD + S - 1) / S + 3) / 4 * 4;            // row width of the receive buffer
-    float* recv = reinterpret_cast<float*>(ring);             // [S][64 heads][W] (ring + P)
-    float* lse_in = reinterpret_cast<float*>(tbl_all);        // [S][64] (the row tables)
+    float* stage_o = reinterpret_cast<float*>(ring);          // [64][512] (the idle ring)
     float* wts = reinterpret_cast<float*>(sQ);                // [S][64] (q is idle now)
     float* inv = wts + kMaxClusterSplits * kHG;               // [64]
-    cluster.sync();
-    if (warp >= 5) {
-      const int sw = warp - 5, quarter = warp & 3, row = quarter * 32 + lane;
+    if (warp != 4) {
+      const int quarter = warp & 3, half = warp < 4 ? 1 : 0;
       const uint32_t t_lane = uint32_t(quarter * 32) << 16;
-#pragma unroll 1
-      for (int half = 0; half < 2; ++half) {
-        float sc[32];
+      float sc[32];
 #pragma unroll
-        for (int h = 0; h < 32; ++h) sc[h] = stats[half * 32 + h];
+      for (int h = 0; h < 32; ++h) sc[h] = stats[half * 32 + h];
+      float* dst = stage_o + half * 32 * kD + quarter * 32 + lane;
 #pragma unroll 1
-        for (int mb = 0; mb < kD / 128; ++mb) {
-          const int dd = mb * 128 + row;
-          const int r = ((dd >> 2) * S + S - 1) / 128;      // owner of dim dd
-          const int off = dd - 4 * (r * 128 / S);
-          float* dst = cluster.map_shared_rank(recv, r) + (me * kHG + half * 32) * W + off;
-          float v[32];
-          tc::tmem_ld32(tmem + t_lane + kOCol + mb * kHG + half * 32, v);
+      for (int mb = 0; mb < kD / 128; mb += 2) {
+        float va[32], vb[32];
+        tc::tmem_ld32x2(tmem + t_lane + kOCol + mb * kHG + half * 32,
+                        tmem + t_lane + kOCol + (mb + 1) * kHG + half * 32, va, vb);
 #pragma unroll
-          for (int h = 0; h < 32; ++h) dst[h * W] = v[h] * sc[h];
+        for (int h = 0; h < 32; ++h) {
+          dst[h * kD + mb * 128] = va[h] * sc[h];
+          dst[h * kD + mb * 128 + 128] = vb[h] * sc[h];
         }
       }
-      if (sw < 2) {
-        const float l = stats[64 + sw * 32 + lane];
-        for (int r = 0; r < S; ++r) cluster.map_shared_rank(lse_in, r)[me * kHG + sw * 32 + lane] = l;
-      }
     }
-    cluster.sync();                                           // every piece has arrived
+    cluster.sync();                                           // every split is staged
     const int h0 = x.hg * kHG;
+    const uint32_t stats_lse = tc::smem_u32(stats + 64);
     if (threadIdx.x < kHG) {
       const int h = threadIdx.x;
+      float l[kMaxClusterSplits];
+#pragma unroll
+      for (int s2 = 0; s2 < kMaxClusterSplits; ++s2)
+        l[s2] = s2 < S ? tc::ld_cluster_f32(tc::mapa_shared(stats_lse + 4 * h, s2)) : -INFINITY;
       float mx = -INFINITY;
-      for (int s2 = 0; s2 < S; ++s2) mx = fmaxf(mx, lse_in[s2 * kHG + h]);
+#pragma unroll
+      for (int s2 = 0; s2 < kMaxClusterSplits; ++s2) mx = fmaxf(mx, l[s2]);
       float tot = 0.f;
-      for (int s2 = 0; s2 < S; ++s2) {
-        const float wv = mx == -INFINITY ? 0.f : expf(lse_in[s2 * kHG + h] - mx);
-        wts[s2 * kHG + h] = wv;
-        tot += wv;
+#pragma unroll
+      for (int s2 = 0; s2 < kMaxClusterSplits; ++s2) {
+        if (s2 < S) {
+          const float wv = mx == -INFINITY ? 0.f : expf(l[s2] - mx);
+          wts[s2 * kHG + h] = wv;
+          tot += wv;
+        }
       }
       inv[h] = tot > 0.f ? 1.f / tot : 0.f;
       if (me == 0 && a.lse) a.lse[(long long)x.r * a.H + h0 + h] = tot > 0.f ? mx + logf(tot) : -INFINITY;
@@ -649,25 +662,53 @@ __global__ void __launch_bounds__(kThreads, 1) attn_decode_tc(const TcArgs a) {
     __syncthreads();
     const int g_lo = me * (kD / 4) / S, g_hi = (me + 1) * (kD / 4) / S;
     const int width = g_hi - g_lo;                            // 4-dim groups of this CTA
-    for (int i = threadIdx.x; i < kHG * width; i += kThreads) {
-      const int h = i / width, g4 = i % width;
-      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-      for (int s2 = 0; s2 < S; ++s2) {
-        const float wv = wts[s2 * kHG + h];
-        const float4 v = *reinterpret_cast<const float4*>(recv + (s2 * kHG + h) * W + 4 * g4);
-        acc.x = fmaf(wv, v.x, acc.x);
-        acc.y = fmaf(wv, v.y, acc.y);
-        acc.z = fmaf(wv, v.z, acc.z);
-        acc.w = fmaf(wv, v.w, acc.w);
+    const int n_out = kHG * width;
+    const uint32_t stage_base = tc::smem_u32(stage_o);
+    // two outputs per thread and pass; every split's loads of both are issued
+    // before the first is used (four splits at a time)
+    for (int i = threadIdx.x; i < n_out; i += 2 * kThreads) {
+      const int i2 = min(i + kThreads, n_out - 1);
+      const int hA = i / width, gA = i % width, hB = i2 / width, gB = i2 % width;
+      const uint32_t offA = stage_base + 4u * uint32_t(hA * kD + 4 * (g_lo + gA));
+      const uint32_t offB = stage_base + 4u * uint32_t(hB * kD + 4 * (g_lo + gB));
+      float4 accA = make_float4(0.f, 0.f, 0.f, 0.f), accB = accA;
+      for (int s0 = 0; s0 < S; s0 += 4) {
+        float4 va[4], vb[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          if (s0 + u < S) {
+            va[u] = tc::ld_cluster_f4(tc::mapa_shared(offA, s0 + u));
+            vb[u] = tc::ld_cluster_f4(tc::mapa_shared(offB, s0 + u));
+          }
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          if (s0 + u < S) {
+            const float wa = wts[(s0 + u) * kHG + hA], wb = wts[(s0 + u) * kHG + hB];
+            accA.x = fmaf(wa, va[u].x, accA.x);
+            accA.y = fmaf(wa, va[u].y, accA.y);
+            accA.z = fmaf(wa, va[u].z, accA.z);
+            accA.w = fmaf(wa, va[u].w, accA.w);
+            accB.x = fmaf(wb, vb[u].x, accB.x);
+            accB.y = fmaf(wb, vb[u].y, accB.y);
+            accB.z = fmaf(wb, vb[u].z, accB.z);
+            accB.w = fmaf(wb, vb[u].w, accB.w);
+          }
+        }
       }
-      const float iv = inv[h];
-      const __nv_bfloat162 lo2 = __floats2bfloat162_rn(acc.x * iv, acc.y * iv);
-      const __nv_bfloat162 hi2 = __floats2bfloat162_rn(acc.z * iv, acc.w * iv);
-      uint2 pk;
-      pk.x = *reinterpret_cast<const uint32_t*>(&lo2);
-      pk.y = *reinterpret_cast<const uint32_t*>(&hi2);
-      *reinterpret_cast<uint2*>(a.o + ((long long)x.r * a.H + h0 + h) * kD + 4 * (g_lo + g4)) = pk;
+      auto put = [&](int h, int g4, const float4& acc) {
+        const float iv = inv[h];
+        const __nv_bfloat162 lo2 = __floats2bfloat162_rn(acc.x * iv, acc.y * iv);
+        const __nv_bfloat162 hi2 = __floats2bfloat162_rn(acc.z * iv, acc.w * iv);
+        uint2 pk;
+        pk.x = *reinterpret_cast<const uint32_t*>(&lo2);
+        pk.y = *reinterpret_cast<const uint32_t*>(&hi2);
+        *reinterpret_cast<uint2*>(a.o + ((long long)x.r * a.H + h0 + h) * kD + 4 * (g_lo + g4)) = pk;
+      };
+      put(hA, gA, accA);
+      if (i + kThreads < n_out) put(hB, gB, accB);
     }
+    cluster.sync();                                           // peers are done reading
   }
   tc::fence_before_sync();
   __syncthreads();
