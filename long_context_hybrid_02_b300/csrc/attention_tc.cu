@@ -79,7 +79,7 @@ constexpr size_t kSmem = 1024 + kQBytes + kSmemRing + kPBytes + kSmemTbl + kSmem
 static_assert(kSmem <= 232448, "shared-memory budget");
 // the in-cluster merge stages o as float32 [64][512] over the ring and keeps its
 // weights [S][64] and 1/sum [64] in q's space
-static_assert(size_t(kHG) * kD * 4 <= kSmemRing, "merge staging");
+static_assert(size_t(kHG) * kD * 2 <= kSmemRing, "merge staging");
 static_assert((kMaxClusterSplits + 1) * kHG * 4 <= kQBytes, "merge weights");
 
 struct TcArgs {
@@ -219,6 +219,12 @@ __device__ __forceinline__ float warp_transpose_reduce32(const float (&v)[32], O
 }
 
 struct MaxOp { __device__ float operator()(float x, float y) const { return fmaxf(x, y); } };
+
+// Four bfloat16 (two 32-bit words, low half first) as floats.
+__device__ __forceinline__ float4 bf16x4_to_f4(uint2 u) {
+  return make_float4(__uint_as_float(u.x << 16), __uint_as_float(u.x & 0xffff0000u),
+                     __uint_as_float(u.y << 16), __uint_as_float(u.y & 0xffff0000u));
+}
 struct AddOp { __device__ float operator()(float x, float y) const { return x + y; } };
 
 __global__ void __launch_bounds__(kThreads, 1) attn_decode_tc(const TcArgs a) {
@@ -601,19 +607,22 @@ __global__ void __launch_bounds__(kThreads, 1) attn_decode_tc(const TcArgs a) {
   __syncthreads();
   if (a.cluster_merge) {
     // Every CTA of the cluster holds one split of the same query row and head group.
-    // Each CTA stages its normalised o as float32 [64 heads][512 dims] over its idle
+    // Each CTA stages its normalised o as bfloat16 [64 heads][512 dims] over its idle
     // ring, with the eight warps that can read its tensor memory (warps 0-3 and 5-8;
-    // lanes = consecutive dims, so every store is one 128-byte row segment).  After
-    // a cluster barrier, CTA r merges the dims [lo(r), lo(r + 1)), lo(r) =
-    // 4 floor(128 r / S), reading every split's o and lse from the peers' shared
-    // memory (16-byte loads, 512 contiguous bytes per warp), in split order:
+    // lanes = consecutive dims).  After a cluster barrier, CTA r merges the dims
+    // [lo(r), lo(r + 1)), lo(r) = 4 floor(128 r / S), reading every split's o and
+    // lse from the peers' shared memory (8-byte loads, 256 contiguous bytes per
+    // warp), in split order and in float32:
     //   o = sum_s exp(lse_s - mx) o_s / sum_s exp(lse_s - mx),  lse = mx + log(sum).
+    // The exchange between SMs is the slow part of the merge (its bandwidth is far
+    // below the SM's own shared memory), so o_s crosses it in bfloat16: o is a convex
+    // combination of the o_s, so the rounding adds at most 2^-9 max_s |o_s|.
     // A last barrier keeps every CTA's shared memory alive until its peers are done.
     tc::fence_after_sync();
     cg::cluster_group cluster = cg::this_cluster();
     const Item x = item_of(a, blockIdx.x);
     const int S = a.S, me = x.split;
-    float* stage_o = reinterpret_cast<float*>(ring);          // [64][512] (the idle ring)
+    bf16* stage_o = reinterpret_cast<bf16*>(ring);            // [64][512] (the idle ring)
     float* wts = reinterpret_cast<float*>(sQ);                // [S][64] (q is idle now)
     float* inv = wts + kMaxClusterSplits * kHG;               // [64]
     if (warp != 4) {
@@ -622,7 +631,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_decode_tc(const TcArgs a) {
       float sc[32];
 #pragma unroll
       for (int h = 0; h < 32; ++h) sc[h] = stats[half * 32 + h];
-      float* dst = stage_o + half * 32 * kD + quarter * 32 + lane;
+      bf16* dst = stage_o + half * 32 * kD + quarter * 32 + lane;
 #pragma unroll 1
       for (int mb = 0; mb < kD / 128; mb += 2) {
         float va[32], vb[32];
@@ -630,8 +639,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_decode_tc(const TcArgs a) {
                         tmem + t_lane + kOCol + (mb + 1) * kHG + half * 32, va, vb);
 #pragma unroll
         for (int h = 0; h < 32; ++h) {
-          dst[h * kD + mb * 128] = va[h] * sc[h];
-          dst[h * kD + mb * 128 + 128] = vb[h] * sc[h];
+          dst[h * kD + mb * 128] = __float2bfloat16_rn(va[h] * sc[h]);
+          dst[h * kD + mb * 128 + 128] = __float2bfloat16_rn(vb[h] * sc[h]);
         }
       }
     }
@@ -669,16 +678,16 @@ __global__ void __launch_bounds__(kThreads, 1) attn_decode_tc(const TcArgs a) {
     for (int i = threadIdx.x; i < n_out; i += 2 * kThreads) {
       const int i2 = min(i + kThreads, n_out - 1);
       const int hA = i / width, gA = i % width, hB = i2 / width, gB = i2 % width;
-      const uint32_t offA = stage_base + 4u * uint32_t(hA * kD + 4 * (g_lo + gA));
-      const uint32_t offB = stage_base + 4u * uint32_t(hB * kD + 4 * (g_lo + gB));
+      const uint32_t offA = stage_base + 2u * uint32_t(hA * kD + 4 * (g_lo + gA));
+      const uint32_t offB = stage_base + 2u * uint32_t(hB * kD + 4 * (g_lo + gB));
       float4 accA = make_float4(0.f, 0.f, 0.f, 0.f), accB = accA;
       for (int s0 = 0; s0 < S; s0 += 4) {
         float4 va[4], vb[4];
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
           if (s0 + u < S) {
-            va[u] = tc::ld_cluster_f4(tc::mapa_shared(offA, s0 + u));
-            vb[u] = tc::ld_cluster_f4(tc::mapa_shared(offB, s0 + u));
+            va[u] = bf16x4_to_f4(tc::ld_cluster_u2(tc::mapa_shared(offA, s0 + u)));
+            vb[u] = bf16x4_to_f4(tc::ld_cluster_u2(tc::mapa_shared(offB, s0 + u)));
           }
         }
 #pragma unroll

@@ -226,6 +226,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int quarter = warp & 3;                     // TMEM lanes 32*quarter ..
     const int row = quarter * 32 + lane;              // entry within the tile
     float* w_mine = s_w + (warp - 2) * QT * kHeads;   // this warp's copy of the weights
+    int ne_q[QT];                                     // eligible entries of the group's queries
+    float w_reg[QT == 1 ? kHeads : 1];                // decode: the weights stay in registers
     int i = 0, prev_g = -1;
     bool ok = true;
     do {
@@ -237,6 +239,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           w_mine[x] = (q0 + q < a.Tq) ? a.w[(long long)(b * a.Tq + q0 + q) * kHeads + x % kHeads] : 0.f;
         }
         __syncwarp();
+#pragma unroll
+        for (int q = 0; q < QT; ++q)
+          ne_q[q] = q0 + q < a.Tq ? n_eligible(a.q_pos[b * a.Tq + q0 + q], a.n_win, a.m, a.elig, a.n_cap) : 0;
+        if constexpr (QT == 1) {
+#pragma unroll
+          for (int h = 0; h < kHeads; ++h) w_reg[h] = w_mine[h];
+        }
         prev_g = walk.g;
       }
       const int acc = i & 1;
@@ -245,20 +254,28 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) break;
       tc::fence_after_sync();
       const int j = walk.t * kTileM + row;
-#pragma unroll 1
-      for (int q = 0; q < QT; ++q) {
+      if constexpr (QT == 1) {
+        float v0[32], v1[32];
+        tc::tmem_ld32x2(tmem + (uint32_t(quarter * 32) << 16) + acc * C::N,
+                        tmem + (uint32_t(quarter * 32) << 16) + acc * C::N + 32, v0, v1);
         float s = 0.f;
 #pragma unroll
-        for (int half = 0; half < 2; ++half) {
-          float v[32];
-          tc::tmem_ld32(tmem + (uint32_t(quarter * 32) << 16) + acc * C::N + q * kHeads + half * 32, v);
+        for (int h = 0; h < 32; ++h) s = fmaf(w_reg[h], fmaxf(v0[h], 0.f), s);
 #pragma unroll
-          for (int h = 0; h < 32; ++h) s = fmaf(w_mine[q * kHeads + half * 32 + h], fmaxf(v[h], 0.f), s);
-        }
-        if (q0 + q < a.Tq) {
-          const long long r = (long long)b * a.Tq + q0 + q;
-          const int ne = n_eligible(a.q_pos[r], a.n_win, a.m, a.elig, a.n_cap);
-          if (j < ne) a.scores[r * a.n_cap + j] = s;
+        for (int h = 0; h < 32; ++h) s = fmaf(w_reg[32 + h], fmaxf(v1[h], 0.f), s);
+        if (j < ne_q[0]) a.scores[((long long)b * a.Tq + q0) * a.n_cap + j] = s;
+      } else {
+#pragma unroll
+        for (int q = 0; q < QT; ++q) {
+          float s = 0.f;
+#pragma unroll
+          for (int half = 0; half < 2; ++half) {
+            float v[32];
+            tc::tmem_ld32(tmem + (uint32_t(quarter * 32) << 16) + acc * C::N + q * kHeads + half * 32, v);
+#pragma unroll
+            for (int h = 0; h < 32; ++h) s = fmaf(w_mine[q * kHeads + half * 32 + h], fmaxf(v[h], 0.f), s);
+          }
+          if (j < ne_q[q]) a.scores[((long long)b * a.Tq + q0 + q) * a.n_cap + j] = s;
         }
       }
       tc::fence_before_sync();

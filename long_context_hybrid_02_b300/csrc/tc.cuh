@@ -274,6 +274,11 @@ __device__ __forceinline__ float4 ld_cluster_f4(uint32_t caddr) {
                : "r"(caddr));
   return v;
 }
+__device__ __forceinline__ uint2 ld_cluster_u2(uint32_t caddr) {
+  uint2 v;
+  asm volatile("ld.shared::cluster.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(caddr));
+  return v;
+}
 __device__ __forceinline__ float ld_cluster_f32(uint32_t caddr) {
   float v;
   asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(caddr));
