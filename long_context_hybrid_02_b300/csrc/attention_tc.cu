@@ -93,15 +93,18 @@ struct TcArgs {
   int decode, Tq, H, n_cap, tok_cap, n_win, m, k, elig;
   float c;               // softmax scale * log2(e)
   int S, kps, HG;
+  int G;                 // cluster groups per (row, head group): consecutive key ranges
   int cluster_merge;     // 1: one item per CTA, splits of a row merged in the cluster
-  long long n_items;     // rows * HG * S
+  long long n_items;     // rows * HG * G * S
   bf16* o;               // [rows, H, 512]
   float* lse;            // [rows, H] or null
+  float* o_part;         // G > 1: float32 [rows, G, H, 512], merged by a second launch
+  float* lse_part;       // G > 1: [rows, G, H]
   int* err;
 };
 
 struct Item {
-  int r, b, hg, split;
+  int r, b, hg, g, split;
   int t;          // query position
   int ne;         // eligible compressed entries
   int n_c, n_w;   // compressed / window slots of the row's key list
@@ -113,11 +116,13 @@ struct Item {
 __device__ __forceinline__ Item item_head(const TcArgs& a, long long it) {
   Item x;
   x.split = int(it % a.S);
-  const long long rest = it / a.S;
+  long long rest = it / a.S;
+  x.g = int(rest % a.G);
+  rest /= a.G;
   x.hg = int(rest % a.HG);
   x.r = int(rest / a.HG);
   x.b = x.r / a.Tq;
-  x.lo = x.split * a.kps;
+  x.lo = (x.g * a.S + x.split) * a.kps;
   return x;
 }
 
@@ -666,7 +671,11 @@ __global__ void __launch_bounds__(kThreads, 1) attn_decode_tc(const TcArgs a) {
         }
       }
       inv[h] = tot > 0.f ? 1.f / tot : 0.f;
-      if (me == 0 && a.lse) a.lse[(long long)x.r * a.H + h0 + h] = tot > 0.f ? mx + logf(tot) : -INFINITY;
+      const float lse_m = tot > 0.f ? mx + logf(tot) : -INFINITY;
+      if (me == 0) {
+        if (a.G > 1) a.lse_part[((long long)x.r * a.G + x.g) * a.H + h0 + h] = lse_m;
+        else if (a.lse) a.lse[(long long)x.r * a.H + h0 + h] = lse_m;
+      }
     }
     __syncthreads();
     const int g_lo = me * (kD / 4) / S, g_hi = (me + 1) * (kD / 4) / S;
@@ -707,6 +716,12 @@ __global__ void __launch_bounds__(kThreads, 1) attn_decode_tc(const TcArgs a) {
       }
       auto put = [&](int h, int g4, const float4& acc) {
         const float iv = inv[h];
+        if (a.G > 1) {                                        // partial of this group
+          *reinterpret_cast<float4*>(a.o_part + (((long long)x.r * a.G + x.g) * a.H + h0 + h) * kD +
+                                     4 * (g_lo + g4)) =
+              make_float4(acc.x * iv, acc.y * iv, acc.z * iv, acc.w * iv);
+          return;
+        }
         const __nv_bfloat162 lo2 = __floats2bfloat162_rn(acc.x * iv, acc.y * iv);
         const __nv_bfloat162 hi2 = __floats2bfloat162_rn(acc.z * iv, acc.w * iv);
         uint2 pk;
@@ -776,6 +791,38 @@ int max_cluster_splits() {
   return best;
 }
 
+// Clusters of S CTAs of this kernel that the device keeps resident at once (0 when
+// the query fails).  Clusters need their SMs inside one GPC, so large clusters
+// pack worse than small ones.
+int active_clusters(int S) {
+  static int cached[64][kMaxClusterSplits + 1] = {};
+  int dev = 0;
+  if (S < 1 || S > kMaxClusterSplits) return 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+  if (cached[dev][S] != 0) return cached[dev][S] > 0 ? cached[dev][S] : 0;
+  int n = 0;
+  if (ensure_smem(reinterpret_cast<const void*>(attn_decode_tc), kSmem) == cudaSuccess &&
+      (S <= 8 || cudaFuncSetAttribute(reinterpret_cast<const void*>(attn_decode_tc),
+                                      cudaFuncAttributeNonPortableClusterSizeAllowed,
+                                      1) == cudaSuccess)) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(unsigned(S));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = kSmem;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = unsigned(S);
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaOccupancyMaxActiveClusters(&n, attn_decode_tc, &cfg) != cudaSuccess) n = 0;
+  }
+  (void)cudaGetLastError();
+  cached[dev][S] = n > 0 ? n : -1;
+  return n > 0 ? n : 0;
+}
+
 AttnPlan plan_attention_tc(const ha_params& p, int rows, int max_keys) {
   AttnPlan pl{};
   const long long units = (long long)rows * (p.H / kHG);
@@ -787,15 +834,35 @@ AttnPlan plan_attention_tc(const ha_params& p, int rows, int max_keys) {
   if (S > kPreferredClusterSplits) S = kPreferredClusterSplits;
   if (S > max_cluster_splits()) S = max_cluster_splits();
   if (S < 1) S = 1;
-  int kps = (max_keys + S - 1) / S;
+  // all clusters resident at once (a second wave would double the time)
+  while (S > 1 && active_clusters(S) > 0 && units > active_clusters(S)) --S;
+  // When the clusters still leave half the GPU idle and every split would walk
+  // more than two tiles (few long rows: HCA at 1M tokens), each row's keys are
+  // cut into G consecutive ranges of one cluster each, clusters of 4 (they pack
+  // into the GPCs better than clusters of 8, of which fewer are resident); the G
+  // cluster results (float32, with their lse) are merged by a second launch.
+  int G = 1;
+  if (S > 1 && units * S * 2 <= sms && (max_keys + S - 1) / S > 2 * kTile) {
+    S = S < 4 ? S : 4;
+    G = int(sms / (units * S));
+    const int fit = active_clusters(S);
+    if (fit > 0 && G > fit / units) G = int(fit / units);
+    const int g_keys = (max_keys + S * 2 * kTile - 1) / (S * 2 * kTile);
+    if (G > g_keys) G = g_keys;
+    if (G < 1) G = 1;
+  }
+  int kps = (max_keys + S * G - 1) / (S * G);
   kps = (kps + 15) / 16 * 16;
   if (kps < 16) kps = 16;
-  S = (max_keys + kps - 1) / kps;
-  if (S < 1) S = 1;
+  if (G == 1) {
+    S = (max_keys + kps - 1) / kps;
+    if (S < 1) S = 1;
+  }
   pl.n_splits = S;
   pl.keys_per_split = kps;
   pl.tile = kTile;
-  pl.ws_bytes = 0;                                      // splits merge inside the kernel
+  pl.n_groups = G;
+  pl.ws_bytes = G > 1 ? size_t(rows) * G * p.H * (kD + 1) * sizeof(float) : 0;
   return pl;
 }
 
@@ -827,18 +894,25 @@ cudaError_t launch_attention_tc(const ha_params& p, const AttnPlan& pl, int deco
   a.kps = pl.keys_per_split;
   a.HG = p.H / kHG;
   const int rows = p.B * Tq;
-  a.n_items = (long long)rows * a.S * a.HG;
+  a.G = pl.n_groups > 1 && a.S > 1 ? pl.n_groups : 1;
+  a.n_items = (long long)rows * a.S * a.G * a.HG;
   a.o = static_cast<bf16*>(o);
   a.lse = lse;
   a.err = err;
   a.cluster_merge = a.S > 1 ? 1 : 0;
-  (void)ws;
+  if (a.G > 1) {
+    if (ws == nullptr) return cudaErrorInvalidValue;
+    a.o_part = static_cast<float*>(ws);
+    a.lse_part = a.o_part + (long long)rows * a.G * p.H * kD;
+  }
   cudaError_t e = ensure_smem(reinterpret_cast<const void*>(attn_decode_tc), kSmem);
   if (e != cudaSuccess) return e;
   const long long grid = a.cluster_merge ? a.n_items                    // one item per CTA
                                          : (a.n_items < num_sms() ? a.n_items : num_sms());
-  return launch_pdl(attn_decode_tc, dim3(unsigned(grid)), dim3(kThreads), kSmem, st,
-                    a.cluster_merge ? unsigned(a.S) : 1u, a);
+  e = launch_pdl(attn_decode_tc, dim3(unsigned(grid)), dim3(kThreads), kSmem, st,
+                 a.cluster_merge ? unsigned(a.S) : 1u, a);
+  if (e != cudaSuccess || a.G == 1) return e;
+  return launch_attn_merge(p, rows, a.G, a.o_part, a.lse_part, o, lse, st);
 }
 
 }  // namespace ha

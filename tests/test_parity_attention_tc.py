@@ -22,6 +22,7 @@ from tests._harness import assert_close, np64
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
 D = 512
+L_LONG = 6144 * 128
 
 
 def _caches(Bn, L, n_cap, seed):
@@ -188,13 +189,16 @@ def test_tc_decode_bitwise_repeatable_and_position_invariant():
     assert torch.equal(o1[0], o1[2]) and torch.equal(l1[0], l1[2])
 
 
-def test_tc_decode_hca_long_rows_need_more_than_eight_splits():
-    """6,144 + 128 keys per row: more splits than one cluster merges, so the split
-    partials go through the merge kernel."""
+@pytest.mark.parametrize("ctx_off", [(0, 77), (0, 77, L_LONG - 200, L_LONG)])
+def test_tc_decode_hca_long_rows_in_several_cluster_groups(ctx_off):
+    """Up to 6,144 + 128 keys per row and few rows: every row's keys are cut into
+    several consecutive ranges of one 8-CTA cluster each, whose float32 results
+    are merged by a second launch; a 200-token and an empty context leave whole
+    ranges without keys."""
     m, n_win, ring = 128, 128, 256
     n_cap = 6144
     L = n_cap * m
-    ctx = [L, L - 77]
+    ctx = [L - off for off in ctx_off]
     Bn = len(ctx)
     s = 1 / math.sqrt(D)
     ck = synth.gaussian((Bn, n_cap, D), DEV, 400, s, torch.bfloat16)
@@ -213,10 +217,13 @@ def test_tc_decode_hca_long_rows_need_more_than_eight_splits():
     CK, CV = np64(ck), np64(cv)
     for b, c in enumerate(ctx):
         t = c - 1
+        if t < 0:
+            assert (np64(o[b]) == 0).all() and np.isneginf(np64(lse[b])).all()
+            continue
         ne = O.n_eligible(t, n_win, m)
         win = O.window_positions(t, n_win)
-        keys = np.concatenate([CK[b, :ne], np64(win_k[b])[win - (L - ring)]])
-        vals = np.concatenate([CV[b, :ne], np64(win_v[b])[win - (L - ring)]])
+        keys = np.concatenate([CK[b, :ne], np64(k_ring[b])[win % ring]])    # the slots read
+        vals = np.concatenate([CV[b, :ne], np64(v_ring[b])[win % ring]])
         ro, rl = O.attend(np64(q[b]), keys, vals, 1 / math.sqrt(D))
         assert_close(np64(o[b]), ro, "bf16", f"o[{b}]")
         assert_close(np64(lse[b]), rl, "bf16", f"lse[{b}]")
