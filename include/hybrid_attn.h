@@ -142,7 +142,9 @@ ha_status csa_index_scores(const ha_params* p, const void* q_idx, const float* w
  * padded with -1:
  *   idx : int32 [B, Tq, k]
  *   ws  : device workspace of ha_workspace_size(p, HA_OP_TOPK, Tq, n_cap) bytes
- *         (may be 0 bytes, then ws may be NULL).
+ *         (0 bytes, ws may be NULL, for n_cap <= 40,960; longer rows are cut
+ *         into segments whose candidate lists go through ws).
+ * n_cap above 41,943,040 (= 40,960 x 1,024) returns HA_ERR_UNSUPPORTED.
  * ------------------------------------------------------------------------- */
 ha_status csa_topk(const ha_params* p, const float* scores, int32_t n_cap,
                    const int32_t* q_pos, int32_t Tq, int32_t* idx, void* ws, size_t ws_bytes,

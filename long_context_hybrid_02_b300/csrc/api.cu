@@ -261,6 +261,8 @@ ha_status csa_topk(const ha_params* p, const float* scores, int32_t n_cap, const
   HA_PTR4(idx);
   HA_OPT_PTR(ws);
   HA_REQUIRE(n_cap >= 1, HA_ERR_INVALID_ARG, "n_cap = %d", n_cap);
+  HA_REQUIRE(n_cap <= ha::topk_max_row_entries(), HA_ERR_UNSUPPORTED, "n_cap = %d > %d", n_cap,
+             ha::topk_max_row_entries());
   HA_REQUIRE(Tq >= 1, HA_ERR_INVALID_ARG, "Tq = %d", Tq);
   HA_REQUIRE((long long)p->B * Tq <= 0x7fffffffLL, HA_ERR_UNSUPPORTED, "B * Tq too large");
   const size_t need = ha::topk_workspace_bytes(*p, Tq, n_cap);

@@ -35,6 +35,7 @@ cudaError_t launch_index_scores_tc(const ha_params& p, const void* q_idx, const 
 
 // topk.cu
 size_t topk_workspace_bytes(const ha_params& p, int Tq, int n_cap);
+int topk_max_row_entries();       // longest score row csa_topk supports
 cudaError_t launch_topk(const ha_params& p, const float* scores, int n_cap, const int32_t* q_pos,
                         int Tq, int32_t* idx, void* ws, size_t ws_bytes, cudaStream_t st);
 

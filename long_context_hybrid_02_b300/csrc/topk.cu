@@ -2,55 +2,27 @@
 // compressed entries are attended, k = 512 for V4-Flash and 1024 for V4-Pro).
 //
 // Exact radix select over order-preserving 32-bit keys of the float scores (NaN
-// ranks as -inf).  A row is handled by a thread-block cluster of C CTAs (C = 1
-// when there are enough rows to fill the GPU, up to 16 for a few long rows); CTA
-// r of the cluster holds the keys of segment r of the row in shared memory.
-//   1. three passes over 11-, 11- and 10-bit digits, most significant first: every
-//      CTA histograms the keys of its segment that still match the selected prefix
-//      (warp-aggregated shared-memory atomics), the C histograms are summed over
-//      distributed shared memory, and every CTA picks the same digit holding the
-//      k-th largest key -> the threshold key T and how many keys equal to T are
-//      needed (`need_eq`);
-//   2. one ordered pass keeps every key > T and the first need_eq keys == T in
-//      index order, which realises the tie rule "larger score, then smaller index"
-//      and writes the result in ascending index order without a sort: each warp
-//      owns a contiguous run of its CTA's segment, counts, and after a block scan
-//      and a cluster-wide exchange of the per-CTA counts writes its selections at
-//      their final positions.
-// Segments longer than the shared-memory budget are re-read from global memory
-// (L2) on every pass.
+// ranks as -inf, -0 as +0), digits of 11, 11 and 10 bits from the top; ties go to
+// the smaller index; the output is in ascending index order.
 //
-// A row of at most kRowMaxKeys entries (decode at up to ~160K tokens, every
-// prefill row of a 128K context) is handled by one 1024-thread CTA instead, with
-// no cluster: the row's keys are loaded into shared memory once, the first-digit
-// histogram is taken from shared memory, the digit passes stop as soon as every
-// key of the selected bin is needed, and the ordered write works on 32-key
-// bitmaps (`selected` = keys above the threshold prefix, `tied` = keys equal to
-// it) whose popcounts are scanned once over the CTA.
-#include <cooperative_groups.h>
-
+// A row of at most kRowMaxKeys entries (decode up to ~160K tokens, every prefill
+// row of a 128K context) is handled by one 1024-thread CTA (topk_row): the keys
+// go to shared memory once; a strided sample of 1,024 keys gives a threshold; the
+// keys at or above it are compacted in index order and the digit passes run on
+// those candidates only, stopping once every key of the selected bin is needed;
+// when the sample misjudged the row the passes run over every key and the write
+// goes through bitmaps of the keys above / equal to the threshold prefix.
+//
+// A longer row (decode at 1M tokens: 262,112 entries) is cut into segments of at
+// most kRowMaxKeys keys (topk_seg, one CTA each, then topk_seg_merge, one CTA per
+// row; see there).  Rows longer than kMaxSegRowKeys are not supported.
 #include "common.cuh"
 #include "kernels.h"
-
-namespace cg = cooperative_groups;
 
 namespace ha {
 namespace {
 
-constexpr int kThreads = 512;
-constexpr int kWarps = kThreads / 32;
 constexpr int kBins = 2048;
-constexpr int kMaxCluster = 16;
-constexpr int kSmemKeys = 40 * 1024;      // keys held in shared memory per CTA
-
-struct TopkShared {
-  int hist[kBins];          // this CTA's histogram of the current pass
-  int hsum[2][kBins];       // cluster-wide histogram, by pass parity
-  int warp_a[kWarps + 1];   // scan scratch
-  int warp_b[kWarps + 1];
-  int sel_digit, sel_above;
-  int cnt_gt, cnt_eq;       // this CTA's counts of keys > T and == T
-};
 
 // Inclusive scan of v over the CTA (NT threads); returns the inclusive prefix and
 // the total in *total.  `scratch` holds NT / 32 + 1 ints.
@@ -312,135 +284,229 @@ __global__ void __launch_bounds__(kRowThreads) topk_row(const float* __restrict_
   }
 }
 
-__global__ void __launch_bounds__(kThreads) topk_cluster(const float* __restrict__ scores,
-                                                         int n_cap, const int32_t* __restrict__ q_pos,
-                                                         int k, int n_win, int m, int elig,
-                                                         int seg_len, int32_t* __restrict__ idx) {
+// ------------------------------------------------------------------ long rows in segments
+// A row longer than one CTA's shared memory holds (decode at 1M tokens: 262,112
+// entries) is cut into segments of at most kRowMaxKeys keys.  topk_seg (one CTA
+// per segment) keeps the keys of its segment at or above a local threshold g_s
+// taken from a strided sample, in index order, in the workspace; topk_seg_merge
+// (one CTA per row) selects the k largest of the row's candidates, which the
+// concatenation of the segments' lists gives in index order.  The result is the
+// row's exact top k whenever the selected threshold prefix is >= every g_s (then
+// no key left out by a segment can be selected); otherwise, or when a list
+// overflows, the row is selected again from all of its scores.
+constexpr int kSegCap = 2048;            // candidates one segment keeps
+constexpr int kMergeCap = 12288;         // candidates of a row the merge holds
+
+struct SegMeta {
+  int count;                             // > kSegCap: the segment's list overflowed
+  uint32_t g;                            // the segment's threshold (0 for an empty segment)
+};
+
+__global__ void __launch_bounds__(kRowThreads) topk_seg(const float* __restrict__ scores,
+                                                       int n_cap, const int32_t* __restrict__ q_pos,
+                                                       int k, int n_win, int m, int elig, int C,
+                                                       int seg_len, SegMeta* __restrict__ meta,
+                                                       uint2* __restrict__ cand) {
   extern __shared__ uint32_t skeys[];
-  __shared__ TopkShared sh;
+  __shared__ RowShared sh;
   pdl_wait_then_release();
-  cg::cluster_group cluster = cg::this_cluster();
-  const int C = int(cluster.num_blocks());
-  const int rank = int(cluster.block_rank());
-  const int row = blockIdx.x / C;
-  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+  const int row = blockIdx.x / C, c = blockIdx.x % C;
+  const int tid = threadIdx.x;
   const int n = n_eligible(q_pos[row], n_win, m, elig, n_cap);
-  int32_t* out = idx + (long long)row * k;
-  if (n <= k) {                                   // uniform over the cluster
-    if (rank == 0)
-      for (int i = tid; i < k; i += kThreads) out[i] = i < n ? i : -1;
+  const int lo = min(n, c * seg_len), hi = min(n, lo + seg_len), len = hi - lo;
+  if (n <= k || len == 0) {                       // nothing to keep
+    if (tid == 0) meta[blockIdx.x] = SegMeta{0, 0u};
     return;
   }
-  const float* s = scores + (long long)row * n_cap;
-  const int lo = min(n, rank * seg_len), hi = min(n, lo + seg_len);
-  const int len = hi - lo;
-  const bool in_smem = len <= kSmemKeys;
-  if (in_smem)
-    for (int i = tid; i < len; i += kThreads) skeys[i] = score_key(s[lo + i]);
-  auto key_at = [&](int i) -> uint32_t { return in_smem ? skeys[i] : score_key(__ldg(s + lo + i)); };
-
-  uint32_t prefix = 0, pmask = 0;
-  int remaining = k;                              // selected keys still to place
-  for (int i = tid; i < kBins; i += kThreads) sh.hsum[0][i] = 0;
+  uint32_t* keys = skeys;                         // key i of the segment at pad32(i)
+  const float* s = scores + (long long)row * n_cap + lo;
+  for (int base = 0; base < len; base += 16 * kRowThreads) {
+    float v[16];
+#pragma unroll
+    for (int u = 0; u < 16; ++u) {
+      const int i = base + u * kRowThreads + tid;
+      v[u] = i < len ? __ldg(s + i) : 0.f;
+    }
+#pragma unroll
+    for (int u = 0; u < 16; ++u) {
+      const int i = base + u * kRowThreads + tid;
+      if (i < len) keys[pad32(i)] = score_key(v[u]);
+    }
+  }
+  __syncthreads();
+  // local threshold: the 22-bit prefix of the sample's t-th largest key, t about
+  // twice the sample's share of the segment's expected part of the top k, plus 16
+  const long long share = ((long long)k * len + n - 1) / n;
+  int srem = int(min(1024LL, 2 * ((share * kRowThreads + len - 1) / len) + 16));
+  const uint32_t skey = keys[pad32(int((long long)tid * len / kRowThreads))];
+  uint32_t g = 0, smask = 0;
 #pragma unroll 1
-  for (int pass = 0; pass < 3; ++pass) {
-    const int shift = pass == 0 ? 21 : (pass == 1 ? 10 : 0);
-    const uint32_t dmask = pass == 2 ? 0x3ffu : 0x7ffu;
-    int* hsum = sh.hsum[pass & 1];
-    // the other buffer was last read by this CTA's previous scan; peers add into it
-    // only after the next cluster barrier
-    for (int i = tid; i < kBins; i += kThreads) { sh.hist[i] = 0; sh.hsum[(pass + 1) & 1][i] = 0; }
+  for (int pass = 0; pass < 2; ++pass) {
+    const int shift = pass == 0 ? 21 : 10;
+    for (int i = tid; i < kBins; i += kRowThreads) sh.hist[i] = 0;
     __syncthreads();
-    for (int base = 0; base < len; base += kThreads) {
-      const int i = base + tid;
-      const bool valid = i < len;
-      const uint32_t key = valid ? key_at(i) : 0u;
-      const bool match = valid && ((key & pmask) == prefix);
-      const unsigned act = __ballot_sync(0xffffffffu, match);
-      if (match) {
-        const uint32_t digit = (key >> shift) & dmask;
-        const unsigned peers = __match_any_sync(act, digit);
-        if (lane == __ffs(peers) - 1) atomicAdd(&sh.hist[digit], __popc(peers));
-      }
-    }
-    if (pass == 0) cluster.sync();                // every peer's hsum[0] is zeroed
-    else __syncthreads();
-    // add this CTA's non-zero bins into every peer's (and its own) sum
-    for (int b = tid; b < kBins; b += kThreads) {
-      const int v = sh.hist[b];
-      if (v != 0)
-        for (int c = 0; c < C; ++c) atomicAdd(cluster.map_shared_rank(hsum, c) + b, v);
-    }
-    cluster.sync();                               // every CTA holds the full histogram
-    // thread t owns bins 2047-4t .. 2044-4t (descending); find the bin where the
-    // running count from the top reaches `remaining`
-    int c4[4], own = 0;
-#pragma unroll
-    for (int q = 0; q < 4; ++q) { c4[q] = hsum[kBins - 1 - 4 * tid - q]; own += c4[q]; }
-    int total;
-    const int incl = block_inclusive_scan<kThreads, int>(own, sh.warp_a, &total);
-    const int excl = incl - own;
-    if (excl < remaining && remaining <= incl) {
-      int run = excl;
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        if (run < remaining && remaining <= run + c4[q]) {
-          sh.sel_digit = kBins - 1 - 4 * tid - q;
-          sh.sel_above = run;
-        }
-        run += c4[q];
-      }
-    }
+    row_hist_add(sh, (skey & smask) == g, (skey >> shift) & 0x7ffu);
     __syncthreads();
-    prefix |= uint32_t(sh.sel_digit) << shift;
-    pmask |= dmask << shift;
-    remaining -= sh.sel_above;
+    row_select_digit(sh, srem);
+    g |= uint32_t(sh.sel_digit) << shift;
+    smask |= 0x7ffu << shift;
+    srem -= sh.sel_above;
     __syncthreads();
   }
-  // prefix is the k-th largest key; `remaining` keys equal to it are taken.
-  const uint32_t thr = prefix;
-  const int need_eq = remaining;
-
-  // ordered pass: warp w owns the contiguous run [w*per_warp, (w+1)*per_warp) of the segment
-  const int per_warp = ((len + kWarps - 1) / kWarps + 31) / 32 * 32;
-  const int w_lo = min(len, wid * per_warp), w_hi = min(len, w_lo + per_warp);
-  int gt = 0, eq = 0;
-  for (int base = w_lo; base < w_hi; base += 32) {
-    const int i = base + lane;
-    const uint32_t key = i < w_hi ? key_at(i) : 0u;
-    gt += __popc(__ballot_sync(0xffffffffu, i < w_hi && key > thr));
-    eq += __popc(__ballot_sync(0xffffffffu, i < w_hi && key == thr));
+  // candidates (keys >= g) in index order: thread t owns [t*kpt, (t+1)*kpt)
+  const int kpt = (len + kRowThreads - 1) / kRowThreads;
+  const int a = min(len, tid * kpt), b = min(len, a + kpt);
+  int own = 0;
+  for (int i = a; i < b; ++i) own += keys[pad32(i)] >= g ? 1 : 0;
+  int total;
+  const int incl = block_inclusive_scan<kRowThreads, int>(own, sh.scratch, &total);
+  if (total <= kSegCap) {
+    uint2* out = cand + (long long)blockIdx.x * kSegCap;
+    int pos = incl - own;
+    for (int i = a; i < b; ++i) {
+      const uint32_t key = keys[pad32(i)];
+      if (key >= g) out[pos++] = make_uint2(key, uint32_t(lo + i));
+    }
   }
-  int gt_tot, eq_tot;
-  const int gt_incl = block_inclusive_scan<kThreads, int>(lane == 0 ? gt : 0, sh.warp_a, &gt_tot);
-  const int eq_incl = block_inclusive_scan<kThreads, int>(lane == 0 ? eq : 0, sh.warp_b, &eq_tot);
-  int gt_before = __shfl_sync(0xffffffffu, gt_incl, 0) - gt;   // within this CTA
-  int eq_before = __shfl_sync(0xffffffffu, eq_incl, 0) - eq;
-  if (tid == 0) { sh.cnt_gt = gt_tot; sh.cnt_eq = eq_tot; }
-  cluster.sync();
-  for (int c = 0; c < rank; ++c) {
-    const TopkShared* o = cluster.map_shared_rank(&sh, c);
-    gt_before += o->cnt_gt;
-    eq_before += o->cnt_eq;
-  }
-  for (int base = w_lo; base < w_hi; base += 32) {
-    const int i = base + lane;
-    const uint32_t key = i < w_hi ? key_at(i) : 0u;
-    const bool is_gt = i < w_hi && key > thr;
-    const bool is_eq = i < w_hi && key == thr;
-    const unsigned bgt = __ballot_sync(0xffffffffu, is_gt);
-    const unsigned beq = __ballot_sync(0xffffffffu, is_eq);
-    const unsigned below = (1u << lane) - 1u;
-    const int my_gt = gt_before + __popc(bgt & below);
-    const int my_eq = eq_before + __popc(beq & below);
-    const int taken_eq = min(my_eq, need_eq);    // equal keys taken before this one
-    if (is_gt) out[my_gt + taken_eq] = lo + i;
-    else if (is_eq && my_eq < need_eq) out[my_gt + my_eq] = lo + i;
-    gt_before += __popc(bgt);
-    eq_before += __popc(beq);
-  }
-  cluster.sync();                                 // keep shared memory alive for remote readers
+  if (tid == 0) meta[blockIdx.x] = SegMeta{total, g};
 }
+
+__global__ void __launch_bounds__(kRowThreads) topk_seg_merge(
+    const float* __restrict__ scores, int n_cap, const int32_t* __restrict__ q_pos, int k,
+    int n_win, int m, int elig, int C, const SegMeta* __restrict__ meta,
+    const uint2* __restrict__ cand, int32_t* __restrict__ idx) {
+  extern __shared__ uint32_t smem[];
+  __shared__ RowShared sh;
+  __shared__ int s_flag;
+  __shared__ uint32_t s_gmax;
+  pdl_wait_then_release();
+  const int row = blockIdx.x, tid = threadIdx.x;
+  const int n = n_eligible(q_pos[row], n_win, m, elig, n_cap);
+  int32_t* out = idx + (long long)row * k;
+  if (n <= k) {
+    for (int i = tid; i < k; i += kRowThreads) out[i] = i < n ? i : -1;
+    return;
+  }
+  uint32_t* ck = smem;                            // candidate keys, in index order
+  int* ci = reinterpret_cast<int*>(smem + kMergeCap);
+  int* seg_off = ci + kMergeCap;                  // [C + 1]
+  if (tid == 0) { s_flag = 1; s_gmax = 0u; }
+  __syncthreads();
+  // segment counts -> offsets (C <= kRowThreads)
+  int cnt = 0;
+  if (tid < C) {
+    const SegMeta mt = meta[(long long)row * C + tid];
+    cnt = mt.count;
+    if (cnt > kSegCap) s_flag = 0;
+    atomicMax(&s_gmax, mt.g);
+  }
+  int total;
+  const int incl = block_inclusive_scan<kRowThreads, int>(min(cnt, kSegCap + 1), sh.scratch, &total);
+  if (tid < C) seg_off[tid] = incl - min(cnt, kSegCap + 1);
+  if (tid == 0) seg_off[C] = total;
+  __syncthreads();
+  const bool lists_ok = s_flag != 0 && total >= k && total <= kMergeCap;   // uniform
+  if (lists_ok) {
+    // every candidate slot finds its segment (binary search over the offsets), so
+    // that all loads of the row's lists are in flight at once
+    for (int base = 0; base < total; base += 4 * kRowThreads) {
+      uint2 v[4];
+      int at[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int pos = base + u * kRowThreads + tid;
+        at[u] = pos;
+        if (pos < total) {
+          int lo_s = 0, hi_s = C - 1;                 // last segment with seg_off <= pos
+          while (lo_s < hi_s) {
+            const int mid = (lo_s + hi_s + 1) >> 1;
+            if (seg_off[mid] <= pos) lo_s = mid; else hi_s = mid - 1;
+          }
+          v[u] = cand[((long long)row * C + lo_s) * kSegCap + (pos - seg_off[lo_s])];
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        if (at[u] < total) {
+          ck[at[u]] = v[u].x;
+          ci[at[u]] = int(v[u].y);
+        }
+      }
+    }
+    __syncthreads();
+    uint32_t prefix, pmask;
+    int need_eq;
+    row_radix(sh, total, k, [&](int i) { return ck[i]; }, prefix, pmask, need_eq);
+    if (prefix >= s_gmax) {                       // uniform: every selectable key is a candidate
+      const int cpt = (total + kRowThreads - 1) / kRowThreads;
+      const int clo = min(total, tid * cpt), chi = min(total, clo + cpt);
+      unsigned cnt_gt = 0, cnt_eq = 0;
+      for (int i = clo; i < chi; ++i) {
+        const uint32_t km = ck[i] & pmask;
+        cnt_gt += km > prefix ? 1u : 0u;
+        cnt_eq += km == prefix ? 1u : 0u;
+      }
+      unsigned tot;
+      const unsigned packed = block_inclusive_scan<kRowThreads, unsigned>(
+          cnt_gt | (cnt_eq << 16), reinterpret_cast<unsigned*>(sh.scratch), &tot);
+      int gt_before = int(packed & 0xffffu) - int(cnt_gt);
+      int eq_before = int(packed >> 16) - int(cnt_eq);
+      for (int i = clo; i < chi; ++i) {
+        const uint32_t km = ck[i] & pmask;
+        if (km > prefix) {
+          out[gt_before + min(eq_before, need_eq)] = ci[i];
+          ++gt_before;
+        } else if (km == prefix) {
+          if (eq_before < need_eq) out[gt_before + eq_before] = ci[i];
+          ++eq_before;
+        }
+      }
+      return;
+    }
+  }
+  // fallback: digit passes over every score of the row (global memory), then an
+  // ordered write over per-thread contiguous ranges
+  const float* s = scores + (long long)row * n_cap;
+  uint32_t prefix, pmask;
+  int need_eq;
+  row_radix(sh, n, k, [&](int i) { return score_key(__ldg(s + i)); }, prefix, pmask, need_eq);
+  const int kpt = (n + kRowThreads - 1) / kRowThreads;
+  const int a = min(n, tid * kpt), b = min(n, a + kpt);
+  int c_gt = 0, c_eq = 0;
+  for (int i = a; i < b; ++i) {
+    const uint32_t km = score_key(__ldg(s + i)) & pmask;
+    c_gt += km > prefix ? 1 : 0;
+    c_eq += km == prefix ? 1 : 0;
+  }
+  int t_gt, t_eq;
+  int gt_before = block_inclusive_scan<kRowThreads, int>(c_gt, sh.scratch, &t_gt) - c_gt;
+  int eq_before = block_inclusive_scan<kRowThreads, int>(c_eq, sh.scratch, &t_eq) - c_eq;
+  for (int i = a; i < b; ++i) {
+    const uint32_t km = score_key(__ldg(s + i)) & pmask;
+    if (km > prefix) {
+      out[gt_before + min(eq_before, need_eq)] = i;
+      ++gt_before;
+    } else if (km == prefix) {
+      if (eq_before < need_eq) out[gt_before + eq_before] = i;
+      ++eq_before;
+    }
+  }
+}
+
+// Segments per row for rows longer than kRowMaxKeys: enough CTAs to cover the GPU,
+// each segment at most kRowMaxKeys keys and a multiple of 32.
+struct SegPlan { int C, seg_len; };
+SegPlan seg_plan(long long rows, int n_cap, int sms) {
+  int C = (n_cap + kRowMaxKeys - 1) / kRowMaxKeys;
+  const long long want = sms / (rows > 0 ? rows : 1);
+  if (want > C) C = int(want < kRowThreads ? want : kRowThreads);
+  int seg = (n_cap + C - 1) / C;
+  seg = (seg + 31) / 32 * 32;
+  if (seg > kRowMaxKeys) seg = kRowMaxKeys;
+  C = (n_cap + seg - 1) / seg;
+  return SegPlan{C, seg};
+}
+constexpr int kMaxSegRowKeys = kRowMaxKeys * kRowThreads;   // longest row supported
 
 int g_num_sms[64] = {};
 
@@ -456,44 +522,19 @@ int num_sms() {
   return g_num_sms[dev];
 }
 
-// Largest cluster the current device can schedule for this kernel with a full
-// shared-memory segment: 16 needs the non-portable cluster size, else 8.
-int max_cluster() {
-  static int cached[64] = {};
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 8;
-  if (cached[dev] != 0) return cached[dev];
-  int best = 8;
-  const size_t smem = size_t(kSmemKeys) * sizeof(uint32_t);
-  if (ensure_smem(reinterpret_cast<const void*>(topk_cluster), smem) == cudaSuccess &&
-      cudaFuncSetAttribute(reinterpret_cast<const void*>(topk_cluster),
-                           cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess) {
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(kMaxCluster);
-    cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = smem;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = kMaxCluster;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, topk_cluster, &cfg) == cudaSuccess && n > 0)
-      best = kMaxCluster;
-  }
-  (void)cudaGetLastError();
-  cached[dev] = best;
-  return best;
-}
-
 }  // namespace
 
-size_t topk_workspace_bytes(const ha_params&, int, int) { return 0; }
+int topk_max_row_entries() { return kMaxSegRowKeys; }
+
+size_t topk_workspace_bytes(const ha_params& p, int Tq, int n_cap) {
+  if (n_cap <= kRowMaxKeys || n_cap > kMaxSegRowKeys) return 0;
+  const long long rows = (long long)p.B * Tq;
+  const SegPlan sp = seg_plan(rows, n_cap, num_sms());
+  return size_t(rows) * sp.C * (sizeof(SegMeta) + size_t(kSegCap) * sizeof(uint2));
+}
 
 cudaError_t launch_topk(const ha_params& p, const float* scores, int n_cap, const int32_t* q_pos,
-                        int Tq, int32_t* idx, void*, size_t, cudaStream_t st) {
+                        int Tq, int32_t* idx, void* ws, size_t ws_bytes, cudaStream_t st) {
   const long long rows = (long long)p.B * Tq;
   if (rows == 0) return cudaSuccess;
   if (n_cap <= kRowMaxKeys) {                     // the row fits one CTA's shared memory
@@ -503,18 +544,26 @@ cudaError_t launch_topk(const ha_params& p, const float* scores, int n_cap, cons
     return launch_pdl(topk_row, dim3(unsigned(rows)), dim3(kRowThreads), smem, st, 1u, scores,
                       n_cap, q_pos, p.k, p.n_win, p.m, p.elig, idx);
   }
-  // CTAs per row: enough to cover the GPU when rows are few, and enough for every
-  // segment to fit the shared-memory budget when possible.
-  const int c_max = max_cluster();
-  int C = 1;
-  while (C < c_max && rows * C < num_sms()) C *= 2;
-  while (C < c_max && (n_cap + C - 1) / C > kSmemKeys) C *= 2;
-  const int seg_len = (n_cap + C - 1) / C;
-  const size_t smem = size_t(seg_len < kSmemKeys ? seg_len : kSmemKeys) * sizeof(uint32_t);
-  cudaError_t e = ensure_smem(reinterpret_cast<const void*>(topk_cluster), smem);
-  if (e != cudaSuccess) return e;
-  return launch_pdl(topk_cluster, dim3(unsigned(rows * C)), dim3(kThreads), smem, st, unsigned(C),
-                    scores, n_cap, q_pos, p.k, p.n_win, p.m, p.elig, seg_len, idx);
+  if (n_cap <= kMaxSegRowKeys) {                  // segments, then one merge per row
+    const SegPlan sp = seg_plan(rows, n_cap, num_sms());
+    const size_t need = size_t(rows) * sp.C * (sizeof(SegMeta) + size_t(kSegCap) * sizeof(uint2));
+    if (ws == nullptr || ws_bytes < need) return cudaErrorInvalidValue;
+    uint2* cand = static_cast<uint2*>(ws);
+    SegMeta* meta = reinterpret_cast<SegMeta*>(cand + size_t(rows) * sp.C * kSegCap);
+    const size_t smem1 = size_t(sp.seg_len / 32) * 33 * sizeof(uint32_t);
+    cudaError_t e = ensure_smem(reinterpret_cast<const void*>(topk_seg), smem1);
+    if (e != cudaSuccess) return e;
+    e = launch_pdl(topk_seg, dim3(unsigned(rows * sp.C)), dim3(kRowThreads), smem1, st, 1u, scores,
+                   n_cap, q_pos, p.k, p.n_win, p.m, p.elig, sp.C, sp.seg_len, meta, cand);
+    if (e != cudaSuccess) return e;
+    const size_t smem2 = (size_t(2) * kMergeCap + sp.C + 1) * sizeof(uint32_t);
+    e = ensure_smem(reinterpret_cast<const void*>(topk_seg_merge), smem2);
+    if (e != cudaSuccess) return e;
+    return launch_pdl(topk_seg_merge, dim3(unsigned(rows)), dim3(kRowThreads), smem2, st, 1u,
+                      scores, n_cap, q_pos, p.k, p.n_win, p.m, p.elig, sp.C,
+                      static_cast<const SegMeta*>(meta), static_cast<const uint2*>(cand), idx);
+  }
+  return cudaErrorNotSupported;                  // rows longer than kMaxSegRowKeys
 }
 
 }  // namespace ha

@@ -83,6 +83,10 @@ def test_index_topk_validation(lib):
     assert code_of(B.csa_topk, P(k=5000), A, 256, A, 1, A, None, 0) == 3
     assert code_of(B.csa_topk, P(dtype=7), A, 256, A, 1, A, None, 0) == 1
     assert code_of(B.csa_topk, P(elig=3), A, 256, A, 1, A, None, 0) == 1
+    assert code_of(B.csa_topk, P(), A, 40960 * 1024 + 1, A, 1, A, None, 0) == 3
+    ws_long = B.ha_workspace_size(P(), B.OP_TOPK, 1, 262144, True)
+    assert ws_long > 0                                   # segment candidate lists
+    assert code_of(B.csa_topk, P(), A, 262144, A, 1, A, (A, ws_long - 1), 0) == 4
 
 
 def test_attention_validation(lib):
@@ -111,7 +115,9 @@ def test_workspace_sizes(lib):
     a = B.ha_workspace_size(P(), B.OP_DECODE, 1, 256, True)
     b = B.ha_workspace_size(P(), B.OP_DECODE, 1, 4096, False)
     assert b >= a > 0
-    assert B.ha_workspace_size(P(), B.OP_TOPK, 1, 256, True) >= 0
+    assert B.ha_workspace_size(P(), B.OP_TOPK, 1, 256, True) == 0      # one CTA per row
+    assert B.ha_workspace_size(P(), B.OP_TOPK, 1, 40960, True) == 0
+    assert B.ha_workspace_size(P(), B.OP_TOPK, 1, 40961, True) > 0
     with pytest.raises(B.HAError):
         B.ha_workspace_size(P(), 9, 1, 256, True)
     with pytest.raises(B.HAError):

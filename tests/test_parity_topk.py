@@ -1,12 +1,13 @@
 """csa_topk against the oracle's selection, bit-exact, in every launch configuration.
 
 Rows of up to 40,960 entries go to one 1024-thread CTA each (keys in shared
-memory, early stop of the digit passes, bitmap-ordered write).  Longer rows are
-split over a cluster of up to 16 CTAs, each holding its segment in shared memory
-up to 40,960 keys and re-reading longer segments from global memory.  The scores
-are fed identically to both sides (float32), so the index sets must be identical:
-ties broken by the smaller index, NaN ranked as -inf, output in ascending index
-order with -1 padding.
+memory, a sampled threshold, early stop of the digit passes).  Longer rows are
+cut into segments of at most 40,960 keys: one CTA per segment keeps the keys at
+or above a local sampled threshold, one CTA per row selects among them, and a
+row whose selection could miss a key (or whose lists overflow) is selected again
+from all of its scores.  The scores are fed identically to both sides
+(float32), so the index sets must be identical: ties broken by the smaller
+index, NaN ranked as -inf, output in ascending index order with -1 padding.
 """
 import numpy as np
 import pytest
@@ -50,8 +51,9 @@ def _scores(shape, seed, ties=None, nans=0):
     return s
 
 
-def test_topk_million_token_rows_in_clusters():
-    """4 rows x 262,144 entries, k = 1024: 8-CTA clusters, 32,768 keys per CTA."""
+def test_topk_million_token_rows_in_segments():
+    """4 rows x 262,144 entries, k = 1024: segments of ~7K keys; heavy ties and an
+    all-equal row overflow the segment lists and take the all-score path."""
     n_cap, k = 262144, 1024
     s = _scores((4, 1, n_cap), 1)
     s[1] = torch.round(s[1] * 8) / 8                        # heavy ties
@@ -62,8 +64,9 @@ def test_topk_million_token_rows_in_clusters():
     _check(s, q_pos, idx, k)
 
 
-def test_topk_segments_beyond_shared_memory():
-    """Segments of 50,000 keys (> 40,960): every radix pass re-reads global memory."""
+def test_topk_long_rows_of_different_lengths():
+    """Rows of 400,000 and 300,000 eligible entries with ties (many segments, the
+    last one ragged)."""
     n_cap, k = 400000, 512
     s = _scores((2, 1, n_cap), 2, ties=16)
     q_pos = torch.tensor([[128 + 4 * n_cap - 1], [128 + 4 * 300000 - 1]], dtype=torch.int32)
@@ -170,5 +173,19 @@ def test_topk_one_cta_sample_blind_rows():
     s[2, 0, :] = 1.0
     q_pos = torch.full((3, 1), 128 + 4 * n_cap - 1, dtype=torch.int32)
     q_pos[2, 0] = 128 + 4 * 3000 - 1                         # 3,000 tied keys
+    idx = _run(s, q_pos, k)
+    _check(s, q_pos, idx, k)
+
+
+def test_topk_long_rows_with_the_top_in_few_segments():
+    """The top k of a long row sits in its first tenth (so the first segments'
+    local thresholds are too high and the row is selected from all its scores),
+    or is planted in 1 % of the entries spread over the row (the sampled path)."""
+    n_cap, k = 150000, 1024
+    g = torch.Generator().manual_seed(33)
+    s = torch.randn((2, 1, n_cap), generator=g)
+    s[0, 0, : n_cap // 10] += 3.0
+    s[1, 0, torch.randperm(n_cap, generator=g)[: n_cap // 100]] += 3.0
+    q_pos = torch.full((2, 1), 128 + 4 * n_cap - 1, dtype=torch.int32)
     idx = _run(s, q_pos, k)
     _check(s, q_pos, idx, k)
