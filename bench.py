@@ -427,6 +427,36 @@ def run_prefill(args, w, dev, world, rank, dist):
     h_out = torch.empty_like(layer.o, device="cpu").pin_memory()
     h2d = sum(x.numel() * x.element_size() for x in h_in.values())
     d2h = h_out.numel() * h_out.element_size()
+    qside = torch.cuda.Stream(device=dev)
+    qfork, qjoin = torch.cuda.Event(), torch.cuda.Event()
+
+    def e2e_step():
+        """The chunk through the public API with its host copies, as one graph: q
+        (read only by the attention) is copied on a branch of its own beside scoring
+        and selection, the indexer's inputs first on the main stream, o back last."""
+        s = stream.cuda_stream
+        qfork.record(stream)
+        qside.wait_event(qfork)
+        with torch.cuda.stream(qside):
+            qry["q"].copy_(h_in["q"], non_blocking=True)
+        qjoin.record(qside)
+        for k in ("qI", "w_idx"):
+            qry[k].copy_(h_in[k], non_blocking=True)
+        B.csa_index_scores(layer.p, qry["qI"], qry["w_idx"], layer.cki, layer.n_cap, qry["q_pos"],
+                           w.Tq, layer.scores, s)
+        B.csa_topk(layer.p, layer.scores, layer.n_cap, qry["q_pos"], w.Tq, layer.idx, ws, s)
+        stream.wait_event(qjoin)
+        B.hybrid_attn_prefill(layer.p, qry["q"], qry["q_pos"], w.Tq, layer.ck, layer.cv,
+                              layer.n_cap, layer.idx, tok["k_tok"], tok["v_tok"], layer.tok_cap,
+                              layer.o, layer.lse, ws, s)
+        h_out.copy_(layer.o, non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        e2e_step()                                  # eager warm-up
+    torch.cuda.synchronize()
+    g_e2e = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g_e2e, stream=stream):
+        e2e_step()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e2e_ms = []
     for i in range(args.steps):
@@ -435,10 +465,7 @@ def run_prefill(args, w, dev, world, rank, dist):
         torch.cuda.synchronize()
         with torch.cuda.stream(stream):
             e0.record(stream)
-            for k in h_in:
-                qry[k].copy_(h_in[k], non_blocking=True)
-            graphs[False].replay()
-            h_out.copy_(layer.o, non_blocking=True)
+            g_e2e.replay()
             e1.record(stream)
         e1.synchronize()
         e2e_ms.append(e0.elapsed_time(e1))
@@ -465,7 +492,10 @@ def run_prefill(args, w, dev, world, rank, dist):
                    "timing": "CUDA events at both ends of a CUDA graph of the step, per step"},
         "clocks": clocks.summary(),
         "e2e": {"value": round(e2e_value, 1), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h},
+                "d2h_bytes_per_step": d2h,
+                "timing": "per step: pinned-host copies of the chunk's inputs, the step and the "
+                          "copy of o back, one graph between CUDA events (q copied beside "
+                          "scoring and selection); L2 flushed before every step"},
         "gpu_launches": int(launches_per_step) * args.steps,
         "roofline": roofline,
         "indexer_tflops": round(idx_tf, 1),
@@ -672,6 +702,58 @@ def main():
     h_out = torch.empty_like(layer.o, device="cpu").pin_memory()
     h2d = sum(t.numel() * t.element_size() for t in h_in.values())
     d2h = h_out.numel() * h_out.element_size()
+    qside = torch.cuda.Stream(device=dev)
+    qfork, qjoin, tok_ready = torch.cuda.Event(), torch.cuda.Event(), torch.cuda.Event()
+    tok_names = [kname for kname in h_in if kname.startswith("new_")]
+    idx_names = [kname for kname in ("qI", "w_idx") if kname in h_in]
+
+    def e2e_step():
+        """One decode step through the public API with its own host copies, as one
+        graph: the query q (read only by the attention) is copied on a branch of its
+        own beside scoring and selection; the new token's rows are copied beside
+        them, ahead of the compression that reads them (the attention waits for
+        them: the window holds the newest token); the indexer's inputs are copied
+        first on the main stream; o is copied back at the end."""
+        s = stream.cuda_stream
+        qfork.record(stream)
+        qside.wait_event(qfork)
+        side.wait_event(qfork)
+        with torch.cuda.stream(qside):
+            d_in["q"].copy_(h_in["q"], non_blocking=True)
+        qjoin.record(qside)
+        with torch.cuda.stream(side):
+            for kname in tok_names:
+                d_in[kname].copy_(h_in[kname], non_blocking=True)
+        tok_ready.record(side)
+        if concurrent_compress:
+            layer.compress(new_blk, 1, side.cuda_stream)
+            join.record(side)
+        for kname in idx_names:
+            d_in[kname].copy_(h_in[kname], non_blocking=True)
+        if not concurrent_compress:
+            stream.wait_event(tok_ready)
+            layer.compress(new_blk, 1, s)
+        if w.kind == "csa":
+            B.csa_index_scores(layer.p, qry["qI"], qry["w_idx"], layer.cki, layer.n_cap,
+                               qry["q_pos"], 1, layer.scores, s)
+            B.csa_topk(layer.p, layer.scores, layer.n_cap, qry["q_pos"], 1, layer.idx,
+                       (layer.ws.data_ptr(), layer.ws.numel()), s)
+        stream.wait_event(qjoin)
+        stream.wait_event(tok_ready)
+        B.hybrid_attn_decode(layer.p, q, layer.ck, layer.cv, layer.n_cap,
+                             layer.idx if w.kind == "csa" else None, tok["k_tok"], tok["v_tok"],
+                             layer.tok_cap, qry["ctx_len"], layer.o, layer.lse,
+                             (layer.ws.data_ptr(), layer.ws.numel()), s)
+        if concurrent_compress:
+            stream.wait_event(join)
+        h_out.copy_(layer.o, non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        e2e_step()                                  # eager warm-up
+    torch.cuda.synchronize()
+    g_e2e = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g_e2e, stream=stream):
+        e2e_step()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e2e_ms = []
     for i in range(args.steps):
@@ -679,10 +761,7 @@ def main():
         torch.cuda.synchronize()
         with torch.cuda.stream(stream):
             e0.record(stream)
-            for kname in h_in:
-                d_in[kname].copy_(h_in[kname], non_blocking=True)
-            graph.replay()
-            h_out.copy_(layer.o, non_blocking=True)
+            g_e2e.replay()
             e1.record(stream)
         e1.synchronize()
         e2e_ms.append(e0.elapsed_time(e1))
@@ -717,7 +796,10 @@ def main():
                    "timing": "CUDA events at both ends of a CUDA graph of the step, per step"},
         "clocks": clk,
         "e2e": {"value": round(e2e_value, 1), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h},
+                "d2h_bytes_per_step": d2h,
+                "timing": "per step: pinned-host copies of the step's inputs, the step and the "
+                          "copy of o back, one graph between CUDA events (q copied beside "
+                          "scoring and selection); L2 flushed before every step"},
         "gpu_launches": int(launches_per_step) * args.steps,
         "roofline": roofline,
         "cpu_baseline": cpu,

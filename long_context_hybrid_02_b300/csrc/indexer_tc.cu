@@ -37,10 +37,17 @@ template <int QT> struct Cfg {
   static constexpr int N = QT * kHeads;
   static constexpr int kStages = QT == 1 ? 6 : (QT == 2 ? 5 : 4);
   static constexpr int kQBytes = N * kDim * 2;
+  // decode: two query buffers, so that a CTA whose tile range crosses into the
+  // next sequence loads that sequence's query while the last tiles of the
+  // previous one are still in flight (one buffer stalled such CTAs by a full DRAM
+  // round trip and made them the kernel's tail)
+  static constexpr int kQBuf = QT == 1 ? 2 : 1;
   static constexpr int kTmemCols = 2 * N < 32 ? 32 : 2 * N;
-  static constexpr size_t kSmem = 1024 + size_t(kStages) * kTileBytes + kQBytes +
+  static constexpr size_t kSmem = 1024 + size_t(kStages) * kTileBytes + size_t(kQBuf) * kQBytes +
                                   4 * QT * kHeads * sizeof(float) + 256;
 };
+
+static_assert(Cfg<1>::kSmem <= 232448 && Cfg<4>::kSmem <= 232448, "shared-memory budget");
 
 struct IdxArgs {
   const float* w;          // [B*Tq, H_I]
@@ -133,16 +140,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   unsigned char* base = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   unsigned char* s_k = base;                                   // kStages x 32 KiB
-  unsigned char* s_q = s_k + size_t(C::kStages) * kTileBytes;  // QT x 16 KiB
-  float* s_w = reinterpret_cast<float*>(s_q + C::kQBytes);     // [4 warps][QT][64]
+  unsigned char* s_q = s_k + size_t(C::kStages) * kTileBytes;  // kQBuf x QT x 16 KiB
+  float* s_w = reinterpret_cast<float*>(s_q + size_t(C::kQBuf) * C::kQBytes);  // [4][QT][64]
   uint64_t* bars = reinterpret_cast<uint64_t*>(s_w + 4 * QT * kHeads);
   uint64_t* full = bars;                   // [kStages]
   uint64_t* empty = full + C::kStages;     // [kStages]
   uint64_t* acc_full = empty + C::kStages; // [2]
   uint64_t* acc_empty = acc_full + 2;      // [2]
-  uint64_t* q_full = acc_empty + 2;
-  uint64_t* q_empty = q_full + 1;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(q_empty + 1);
+  uint64_t* q_full = acc_empty + 2;        // [kQBuf]
+  uint64_t* q_empty = q_full + C::kQBuf;   // [kQBuf]
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(q_empty + C::kQBuf);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   TileWalk<QT> walk;
@@ -152,8 +159,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::kStages; ++s) { tc::mbar_init(&full[s], 1); tc::mbar_init(&empty[s], 1); }
     for (int i = 0; i < 2; ++i) { tc::mbar_init(&acc_full[i], 1); tc::mbar_init(&acc_empty[i], 4); }
-    tc::mbar_init(q_full, 1);
-    tc::mbar_init(q_empty, 1);
+    for (int i = 0; i < C::kQBuf; ++i) { tc::mbar_init(&q_full[i], 1); tc::mbar_init(&q_empty[i], 1); }
     tc::fence_mbar_init();
   }
   if (warp == 1) { tc::tmem_alloc(tmem_slot, C::kTmemCols); tc::tmem_relinquish(); }
@@ -171,12 +177,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       int i = 0, prev_g = -1, n_groups_seen = 0;
       do {
         if (walk.g != prev_g) {
-          if (prev_g >= 0 && !tc::mbar_wait(q_empty, (n_groups_seen - 1) & 1, a.err, 11)) break;
+          // group j uses buffer j % kQBuf once group j - kQBuf has released it
+          const int qb = n_groups_seen % C::kQBuf, use = n_groups_seen / C::kQBuf;
+          if (use > 0 && !tc::mbar_wait(&q_empty[qb], (use - 1) & 1, a.err, 11)) break;
           const int b = walk.g / gpb, q0 = (walk.g % gpb) * QT;
           const int y = (b * a.Tq + q0) * kHeads;
-          tc::mbar_expect_tx(q_full, C::kQBytes);
-          tc::tma_load_2d(s_q, &map_q, 0, y, q_full);
-          tc::tma_load_2d(s_q + C::kQBytes / 2, &map_q, 64, y, q_full);
+          unsigned char* qdst = s_q + size_t(qb) * C::kQBytes;
+          tc::mbar_expect_tx(&q_full[qb], C::kQBytes);
+          tc::tma_load_2d(qdst, &map_q, 0, y, &q_full[qb]);
+          tc::tma_load_2d(qdst + C::kQBytes / 2, &map_q, 64, y, &q_full[qb]);
           prev_g = walk.g;
           ++n_groups_seen;
         }
@@ -195,11 +204,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       constexpr uint32_t idesc = tc::idesc_bf16_f32(kTileM, C::N);
-      const uint32_t k_base = tc::smem_u32(s_k), q_base = tc::smem_u32(s_q);
-      int i = 0, prev_g = -1, n_groups_seen = 0;
+      const uint32_t k_base = tc::smem_u32(s_k);
+      uint32_t q_base = tc::smem_u32(s_q);
+      int i = 0, prev_g = -1, n_groups_seen = 0, qb = 0;
       do {
         if (walk.g != prev_g) {
-          if (!tc::mbar_wait(q_full, n_groups_seen & 1, a.err, 21)) break;
+          qb = n_groups_seen % C::kQBuf;
+          if (!tc::mbar_wait(&q_full[qb], (n_groups_seen / C::kQBuf) & 1, a.err, 21)) break;
+          q_base = tc::smem_u32(s_q + size_t(qb) * C::kQBytes);
           prev_g = walk.g;
           ++n_groups_seen;
         }
@@ -217,7 +229,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tc::mma_commit(&empty[s]);
         tc::mma_commit(&acc_full[acc]);
-        if (walk.last_of_group()) tc::mma_commit(q_empty);
+        if (walk.last_of_group()) tc::mma_commit(&q_empty[qb]);
         ++i;
       } while (walk.next(a));
     }
