@@ -428,28 +428,47 @@ def run_prefill(args, w, dev, world, rank, dist):
     h2d = sum(x.numel() * x.element_size() for x in h_in.values())
     d2h = h_out.numel() * h_out.element_size()
     qside = torch.cuda.Stream(device=dev)
-    qfork, qjoin = torch.cuda.Event(), torch.cuda.Event()
+    oside = torch.cuda.Stream(device=dev)
+    n_sub = 4 if w.B == 1 and w.Tq % 4 == 0 else 1      # attention sub-chunks (B = 1: contiguous)
+    sub = w.Tq // n_sub
+    qfork = torch.cuda.Event()
+    q_ready = [torch.cuda.Event() for _ in range(n_sub)]
+    o_ready = [torch.cuda.Event() for _ in range(n_sub)]
+    o_done = torch.cuda.Event()
 
     def e2e_step():
-        """The chunk through the public API with its host copies, as one graph: q
-        (read only by the attention) is copied on a branch of its own beside scoring
-        and selection, the indexer's inputs first on the main stream, o back last."""
+        """The chunk through the public API with its host copies, as one graph.  The
+        indexer's inputs are copied first; scoring and selection run over the whole
+        chunk; the attention runs in sub-chunks of queries (the same call on a range
+        of rows), each starting once its part of q has arrived (q is copied on a
+        branch of its own from the start) and each sending its part of o back on
+        another branch while the next sub-chunk computes."""
         s = stream.cuda_stream
         qfork.record(stream)
         qside.wait_event(qfork)
         with torch.cuda.stream(qside):
-            qry["q"].copy_(h_in["q"], non_blocking=True)
-        qjoin.record(qside)
+            for c in range(n_sub):
+                qry["q"][:, c * sub:(c + 1) * sub].copy_(h_in["q"][:, c * sub:(c + 1) * sub],
+                                                         non_blocking=True)
+                q_ready[c].record(qside)
         for k in ("qI", "w_idx"):
             qry[k].copy_(h_in[k], non_blocking=True)
         B.csa_index_scores(layer.p, qry["qI"], qry["w_idx"], layer.cki, layer.n_cap, qry["q_pos"],
                            w.Tq, layer.scores, s)
         B.csa_topk(layer.p, layer.scores, layer.n_cap, qry["q_pos"], w.Tq, layer.idx, ws, s)
-        stream.wait_event(qjoin)
-        B.hybrid_attn_prefill(layer.p, qry["q"], qry["q_pos"], w.Tq, layer.ck, layer.cv,
-                              layer.n_cap, layer.idx, tok["k_tok"], tok["v_tok"], layer.tok_cap,
-                              layer.o, layer.lse, ws, s)
-        h_out.copy_(layer.o, non_blocking=True)
+        for c in range(n_sub):
+            r = slice(c * sub, (c + 1) * sub)
+            stream.wait_event(q_ready[c])
+            B.hybrid_attn_prefill(layer.p, qry["q"][:, r], qry["q_pos"][:, r], sub, layer.ck,
+                                  layer.cv, layer.n_cap, layer.idx[:, r], tok["k_tok"],
+                                  tok["v_tok"], layer.tok_cap, layer.o[:, r], layer.lse[:, r],
+                                  ws, s)
+            o_ready[c].record(stream)
+            oside.wait_event(o_ready[c])
+            with torch.cuda.stream(oside):
+                h_out[:, r].copy_(layer.o[:, r], non_blocking=True)
+        o_done.record(oside)
+        stream.wait_event(o_done)
 
     with torch.cuda.stream(stream):
         e2e_step()                                  # eager warm-up
@@ -494,8 +513,9 @@ def run_prefill(args, w, dev, world, rank, dist):
         "e2e": {"value": round(e2e_value, 1), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h,
                 "timing": "per step: pinned-host copies of the chunk's inputs, the step and the "
-                          "copy of o back, one graph between CUDA events (q copied beside "
-                          "scoring and selection); L2 flushed before every step"},
+                          "copy of o back, one graph between CUDA events; q copied beside "
+                          "scoring and selection, attention in 4 sub-chunks of queries whose "
+                          "outputs are copied back beside the next; L2 flushed before every step"},
         "gpu_launches": int(launches_per_step) * args.steps,
         "roofline": roofline,
         "indexer_tflops": round(idx_tf, 1),
