@@ -144,6 +144,16 @@ class ClockSampler:
 
 
 # ----------------------------------------------------------------------------- helpers
+def max_over_ranks(value: float, dev, dist, world: int) -> float:
+    """The largest of every rank's `value` (timed milliseconds): the job is as slow as
+    its slowest replica."""
+    import torch
+    t = torch.tensor([float(value)], dtype=torch.float64, device=dev)
+    if world > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 def peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -395,11 +405,8 @@ def run_prefill(args, w, dev, world, rank, dist):
         t_wall = time.perf_counter() - t_wall0
     if world > 1:
         dist.barrier()
-    t_max = torch.tensor([sum(tot)], dtype=torch.float64, device=dev)
-    if world > 1:
-        dist.all_reduce(t_max, op=dist.ReduceOp.MAX)
     tokens = w.B * w.Tq * world * args.steps
-    value = tokens / (float(t_max.item()) / 1e3)
+    value = tokens / (max_over_ranks(sum(tot), dev, dist, world) / 1e3)
     step_ms = sum(tot) / len(tot)
     tot_marked, per = timed(graphs[True], args.steps)
     kern_ms = {n: sum(p[j] for p in per) / len(per) for j, n in enumerate(names)}
@@ -488,7 +495,7 @@ def run_prefill(args, w, dev, world, rank, dist):
             e1.record(stream)
         e1.synchronize()
         e2e_ms.append(e0.elapsed_time(e1))
-    e2e_value = w.B * w.Tq * world * args.steps / (sum(e2e_ms) / 1e3)
+    e2e_value = w.B * w.Tq * world * args.steps / (max_over_ranks(sum(e2e_ms), dev, dist, world) / 1e3)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -678,10 +685,7 @@ def main():
         dist.barrier()
     torch.cuda.synchronize()
     step_ms = sum(tot) / len(tot)
-    t_max = torch.tensor([sum(tot)], dtype=torch.float64, device=dev)
-    if world > 1:
-        dist.all_reduce(t_max, op=dist.ReduceOp.MAX)
-    total_ms = float(t_max.item())
+    total_ms = max_over_ranks(sum(tot), dev, dist, world)
     tokens = w.B * world * args.steps
     value = tokens / (total_ms / 1e3)
     # per-kernel breakdown: the same steps with an event between every two calls
@@ -785,10 +789,7 @@ def main():
             e1.record(stream)
         e1.synchronize()
         e2e_ms.append(e0.elapsed_time(e1))
-    e2e_t = torch.tensor([sum(e2e_ms)], dtype=torch.float64, device=dev)
-    if world > 1:
-        dist.all_reduce(e2e_t, op=dist.ReduceOp.MAX)
-    e2e_value = tokens / (float(e2e_t.item()) / 1e3)
+    e2e_value = tokens / (max_over_ranks(sum(e2e_ms), dev, dist, world) / 1e3)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
