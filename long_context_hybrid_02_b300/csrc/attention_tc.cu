@@ -36,10 +36,11 @@
 //   warps 5-8  softmax of each tile (TMEM lane = key), O^T rescaling, and at the
 //              end of the item the epilogue (TMEM lane = head dim).
 // Rows with one split: persistent grid (one CTA per SM) looping over items.  Rows
-// with 2..16 splits: one item per CTA and the splits of a row form a thread-block
+// with 2..8 splits: one item per CTA and the splits of a row form a thread-block
 // cluster; every CTA stages its normalised o in its own shared memory and merges
 // the head dims it owns by reading every split's o from its peers' shared memory
-// (no workspace, no second launch).
+// (no workspace, no second launch).  Few long rows are cut into G consecutive key
+// ranges of one cluster each, whose float32 results attn_merge combines.
 // Every wait is bounded (tc::kWaitLimitNs); on timeout the kernel records an error
 // code in the library's device error word and returns.
 #include <cooperative_groups.h>
