@@ -110,6 +110,22 @@ def test_attention_validation(lib):
                    None, 0) == 2
 
 
+def test_attention_workspace_only_for_cluster_groups(lib):
+    """The tensor-core decode attention merges a row's splits inside one cluster
+    (no workspace) unless few long rows are cut into several cluster groups,
+    whose float32 results (o and lse per head) go through the workspace.  On a
+    machine without a GPU the plan assumes 148 SMs, as on the B300."""
+    def ws(Bn, H, n_cap, csa):
+        p = B.make_params(Bn, H, 512, 128, 4 if csa else 128, 1024 if csa else 1,
+                          64 if csa else 1, 128 if csa else 8, B.BF16)
+        return B.ha_workspace_size(p, B.OP_DECODE, 1, n_cap, csa)
+    assert ws(32, 64, 16384, True) == 0          # 64K CSA: 32 rows x 4 splits
+    assert ws(32, 64, 1024, False) == 0          # 128K HCA
+    assert ws(4, 128, 262144, True) == 0         # 1M CSA: 1,152 keys, 8 splits
+    # 1M HCA: 8 units x 4 groups of 4-CTA clusters; rows x G x H x (512 + 1) floats
+    assert ws(4, 128, 8192, False) == 4 * 4 * 128 * 513 * 4
+
+
 def test_workspace_sizes(lib):
     # decode partials grow with the key list; HCA lists are n_cap + n_win long
     a = B.ha_workspace_size(P(), B.OP_DECODE, 1, 256, True)
