@@ -85,7 +85,9 @@ def test_index_topk_validation(lib):
     assert code_of(B.csa_topk, P(elig=3), A, 256, A, 1, A, None, 0) == 1
     assert code_of(B.csa_topk, P(), A, 40960 * 1024 + 1, A, 1, A, None, 0) == 3
     ws_long = B.ha_workspace_size(P(), B.OP_TOPK, 1, 262144, True)
-    assert ws_long > 0                                   # segment candidate lists
+    # 2 rows cut into 148 segments in all (one CTA per SM on a B300), each with a
+    # (count, threshold) pair and a list of at most 2,048 (key, index) candidates
+    assert ws_long == 148 * (8 + 2048 * 8)
     assert code_of(B.csa_topk, P(), A, 262144, A, 1, A, (A, ws_long - 1), 0) == 4
 
 
