@@ -54,7 +54,8 @@ import math
 import numpy as np
 
 __all__ = [
-    "round_to_bf16", "round_to_storage", "gate_softmax", "compress_block",
+    "round_to_bf16", "round_to_storage", "round_to_e4m3", "fp8_kv_encode", "fp8_kv_decode",
+    "gate_softmax", "compress_block",
     "compress", "n_eligible", "window_positions", "index_scores", "topk_select",
     "attend", "merge_partials", "csa_decode", "hca_decode", "prefill_query",
 ]
@@ -84,6 +85,58 @@ def round_to_storage(x, storage: str):
     if storage == "f32":
         return np.asarray(x, dtype=np.float64).astype(np.float32).astype(np.float64)
     raise ValueError(f"unknown storage type {storage!r}")
+
+
+# --------------------------------------------------------------------------
+# the deployed KV format ([V4-notes] §8: the KV cache keeps its RoPE dims in BF16
+# and its other dims in FP8).  The page names the split, not the layout; the
+# reading used here: a K or V row of d = 512 dims keeps dims 0..63 (the RoPE
+# dims) as bfloat16 and stores dims 64..511 as float8 e4m3fn values with one
+# float32 scale per group of 64 dims, scale = max|x| / 448 over the group (so the
+# largest element maps to the largest e4m3 value), codes rounded to nearest,
+# ties to even; a row takes 128 + 448 + 28 = 604 bytes instead of 1,024.
+# --------------------------------------------------------------------------
+E4M3_MAX = 448.0            # 1.75 * 2**8, the largest finite e4m3fn value
+FP8_ROPE_DIMS = 64
+FP8_GROUP = 64
+
+
+def round_to_e4m3(x):
+    """Round float64 values to the nearest float8 e4m3fn value, ties to even.
+
+    e4m3fn: sign, 4 exponent bits (bias 7), 3 mantissa bits, no infinity.  Normal
+    values (1 + M/8) * 2**(E-7) for E = 1..15 (E = 15, M = 7 is NaN), so 2**-6 ..
+    448; subnormals k * 2**-9, k = 1..7.  Magnitudes that round above 448 give
+    NaN, as does NaN.
+    """
+    x = np.asarray(x, dtype=np.float64)
+    a = np.abs(x)
+    _, expo = np.frexp(a)                        # a = mant * 2**expo, mant in [0.5, 1)
+    e = np.maximum(expo - 1, -6)                 # exponent of the leading bit; subnormals share -6
+    step = np.ldexp(1.0, e - 3)                  # spacing of the 3-bit mantissa grid
+    q = np.rint(a / step) * step                 # rint: ties to the even grid point
+    q = np.where(q > E4M3_MAX, np.nan, q)
+    q = np.where(np.isnan(x), np.nan, q)
+    return np.copysign(q, x)
+
+
+def fp8_kv_encode(row):
+    """One K or V row in the FP8 format: (RoPE dims as bf16 [64], e4m3 codes
+    [448 // 64, 64] as float64 values, float32 scales [448 // 64])."""
+    row = np.asarray(row, dtype=np.float64)
+    rope = round_to_bf16(row[:FP8_ROPE_DIMS])
+    rest = row[FP8_ROPE_DIMS:].reshape(-1, FP8_GROUP)
+    scale = (np.abs(rest).max(axis=1) / E4M3_MAX).astype(np.float32).astype(np.float64)
+    safe = np.where(scale > 0, scale, 1.0)
+    codes = round_to_e4m3(rest / safe[:, None])
+    codes[scale == 0] = 0.0
+    return rope, codes, scale
+
+
+def fp8_kv_decode(rope, codes, scale):
+    """The row a FP8-format entry stands for (float64): RoPE dims, then code * scale."""
+    return np.concatenate([np.asarray(rope, np.float64),
+                           (np.asarray(codes, np.float64) * np.asarray(scale, np.float64)[:, None]).reshape(-1)])
 
 
 # --------------------------------------------------------------------------

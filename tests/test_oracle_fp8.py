@@ -1,0 +1,91 @@
+"""Pins of the oracle's FP8 KV format ("DeepSeek-V4 深度研究剖析" §8: RoPE dims in
+BF16, the other dims in FP8), independent of the oracle's own arithmetic:
+
+* the e4m3fn grid enumerated from its bit fields: every finite value rounds to
+  itself, every midpoint between neighbours rounds to the one with the even
+  mantissa, values past the largest finite one give NaN;
+* a library routine: torch's float32 -> float8_e4m3fn cast on in-range values;
+* the format's error bound on whole rows: RoPE dims exactly bf16-rounded, every
+  other dim within half a mantissa step (2**-4 relative, or 2**-10 * scale in
+  the subnormal range) of the input, the largest element of a group exact up
+  to the float32 rounding of its scale.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+
+
+def e4m3_grid():
+    """All finite non-negative e4m3fn values with their mantissa field, ascending."""
+    vals = []
+    for E in range(16):
+        for M in range(8):
+            if E == 15 and M == 7:
+                continue                                       # the NaN encoding
+            v = M / 8 * 2.0 ** -6 if E == 0 else (1 + M / 8) * 2.0 ** (E - 7)
+            vals.append((v, M))
+    vals.sort()
+    return vals
+
+
+def test_e4m3_grid_round_trips():
+    grid = e4m3_grid()
+    assert len(grid) == 127 and grid[-1][0] == 448.0 and grid[1][0] == 2.0 ** -9
+    v = np.array([g for g, _ in grid])
+    np.testing.assert_array_equal(O.round_to_e4m3(v), v)
+    np.testing.assert_array_equal(O.round_to_e4m3(-v), -v)
+
+
+def test_e4m3_midpoints_round_to_even_mantissa():
+    grid = e4m3_grid()
+    for (lo, m_lo), (hi, m_hi) in zip(grid[:-1], grid[1:]):
+        mid = (lo + hi) / 2
+        want = lo if m_lo % 2 == 0 else hi
+        assert O.round_to_e4m3(mid) == want, (lo, hi)
+        assert O.round_to_e4m3(math.nextafter(mid, 0)) == lo
+        assert O.round_to_e4m3(math.nextafter(mid, math.inf)) == hi
+
+
+def test_e4m3_overflow_and_nan():
+    out = O.round_to_e4m3(np.array([460.0, 464.0, 470.0, 480.0, 1e6, np.inf, np.nan]))
+    assert out[0] == 448.0 and out[1] == 448.0                # 464 is a tie: 448 has M = 6
+    assert np.isnan(out[2:]).all()
+
+
+def test_e4m3_matches_torch_cast():
+    rng = np.random.default_rng(40)
+    mag = np.exp(rng.uniform(math.log(2.0 ** -12), math.log(447.0), 20000))
+    x = (mag * rng.choice([-1.0, 1.0], mag.size)).astype(np.float32)
+    ref = torch.from_numpy(x).to(torch.float8_e4m3fn).float().numpy().astype(np.float64)
+    np.testing.assert_array_equal(O.round_to_e4m3(x.astype(np.float64)), ref)
+
+
+@pytest.mark.parametrize("seed", [0, 1, 2])
+def test_fp8_kv_row_error_bound(seed):
+    rng = np.random.default_rng(50 + seed)
+    row = rng.standard_normal(512) / math.sqrt(512)
+    row[64 + 64 * 3:64 + 64 * 4] = 0.0                         # an all-zero group
+    rope, codes, scale = O.fp8_kv_encode(row)
+    assert rope.shape == (64,) and codes.shape == (7, 64) and scale.shape == (7,)
+    np.testing.assert_array_equal(rope, O.round_to_bf16(row[:64]))
+    dec = O.fp8_kv_decode(rope, codes, scale)
+    rest, drest = row[64:].reshape(7, 64), dec[64:].reshape(7, 64)
+    assert scale[3] == 0.0 and (drest[3] == 0.0).all()
+    bound = np.maximum(2.0 ** -4 * np.abs(rest), 2.0 ** -10 * scale[:, None]) * (1 + 2.0 ** -20)
+    assert (np.abs(drest - rest) <= bound).all()
+    for g in range(7):
+        if scale[g] > 0:
+            j = np.argmax(np.abs(rest[g]))
+            assert abs(drest[g, j] - rest[g, j]) <= 2.0 ** -22 * abs(rest[g, j])
+
+
+def test_fp8_kv_constant_row():
+    row = np.full(512, -0.0371)
+    rope, codes, scale = O.fp8_kv_encode(row)
+    assert (codes == -448.0).all()
+    dec = O.fp8_kv_decode(rope, codes, scale)
+    assert np.abs(dec[64:] - row[64:]).max() <= 2.0 ** -23 * 0.0371
