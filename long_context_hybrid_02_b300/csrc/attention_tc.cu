@@ -78,7 +78,7 @@ constexpr size_t kSmemTbl = size_t(4) * 2 * kTile * 4;           // [warp][tile 
 constexpr size_t kSmemMisc = (4 * 64 + 64 + 64 + 2 * 64) * 4 + 32 * 8 + 16;
 constexpr size_t kSmem = 1024 + kQBytes + kSmemRing + kPBytes + kSmemTbl + kSmemMisc;
 static_assert(kSmem <= 232448, "shared-memory budget");
-// the in-cluster merge stages o as float32 [64][512] over the ring and keeps its
+// the in-cluster merge stages o as bfloat16 [64][512] over the ring and keeps its
 // weights [S][64] and 1/sum [64] in q's space
 static_assert(size_t(kHG) * kD * 2 <= kSmemRing, "merge staging");
 static_assert((kMaxClusterSplits + 1) * kHG * 4 <= kQBytes, "merge weights");
