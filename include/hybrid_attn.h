@@ -66,7 +66,7 @@ typedef struct CUstream_st* ha_stream_t; /* same handle as cudaStream_t */
 typedef enum {
   HA_OK = 0,
   HA_ERR_INVALID_ARG = 1, /* a size or pointer is out of range / NULL        */
-  HA_ERR_MISALIGNED = 2,  /* a pointer is not 16-byte aligned                */
+  HA_ERR_MISALIGNED = 2,  /* a pointer breaks its alignment rule (16 / 4 B)  */
   HA_ERR_UNSUPPORTED = 3, /* a shape outside the limits below                */
   HA_ERR_WORKSPACE = 4,   /* ws is NULL or smaller than ha_workspace_size()  */
   HA_ERR_CUDA = 5         /* a CUDA runtime call or a launch failed          */

@@ -189,7 +189,7 @@ const char* ha_status_string(ha_status s) {
   switch (s) {
     case HA_OK: return "ok";
     case HA_ERR_INVALID_ARG: return "invalid argument";
-    case HA_ERR_MISALIGNED: return "pointer not 16-byte aligned";
+    case HA_ERR_MISALIGNED: return "pointer misaligned (16 bytes for tensors, 4 for scalar arrays)";
     case HA_ERR_UNSUPPORTED: return "shape outside the supported limits";
     case HA_ERR_WORKSPACE: return "workspace missing or too small";
     case HA_ERR_CUDA: return "CUDA error";
