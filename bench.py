@@ -154,6 +154,9 @@ def max_over_ranks(value: float, dev, dist, world: int) -> float:
     return float(t.item())
 
 
+NOMINAL_HBM_GBS = 7700.0       # B300 HBM3e, nominal
+
+
 def peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -526,6 +529,8 @@ def run_prefill(args, w, dev, world, rank, dist):
         "gpu_launches": int(launches_per_step) * args.steps,
         "roofline": roofline,
         "indexer_tflops": round(idx_tf, 1),
+        "indexer_frac_of_sustained": (round(idx_tf / pk["bf16_tflops_sustained"], 4)
+                                      if pk.get("bf16_tflops_sustained") else None),
         "cpu_baseline": cpu,
         "kernel_ms": {k: round(v, 5) for k, v in kern_ms.items()},
         "ms_per_step_with_kernel_events": round(sum(tot_marked) / len(tot_marked), 5),
@@ -705,7 +710,12 @@ def main():
     roofline = {"bound": "hbm", "kernel": dom, "achieved": round(achieved, 1),
                 "peak": pk["hbm_gbs"], "unit": "GB/s", "frac": round(achieved / pk["hbm_gbs"], 4),
                 "traffic": traffic, "algorithmic_bytes": nbytes[dom],
-                "peak_source": pk["source"] + " (MEASURED_PEAKS.json hbm_gbs)"}
+                "peak_source": pk["source"] + " (MEASURED_PEAKS.json hbm_gbs)",
+                # the same launch on the DRAM bytes ncu counted, and against the
+                # part's nominal 7.7 TB/s
+                "dram_gbs": (round(traffic / (kern_ms[dom] * 1e-3) / 1e9, 1)
+                             if traffic is not None else None),
+                "frac_of_nominal": round(achieved / NOMINAL_HBM_GBS, 4)}
 
     # ---- end to end through the public API: pinned host inputs -> step -> host output
     es = 2 if w.dtype == "bf16" else 4
