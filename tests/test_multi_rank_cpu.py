@@ -51,7 +51,7 @@ def test_replica_timing_is_the_slowest_rank():
     assert out[0] == out[1] == 7.5
 
 
-# one CSA decode query, tiny sizes (config 1 scale)
+# one CSA decode query at small sizes (2,048 tokens, 8 heads of 64 dims)
 L, D, H, H_I, D_I, M, N_WIN, K = 2048, 64, 8, 2, 32, 4, 128, 16
 
 
