@@ -1,6 +1,6 @@
 """Build libhybridattn.so in-tree with nvcc for sm_103a (B300).
 
-Usage: python -m long_context_hybrid_02_b300.build [--force] [--debug]
+Usage: python -m long_context_hybrid_02_b300.build [--force]
 Objects go to _build/ at the repository root; the shared library is written next
 to this file so that it travels with the source tree.
 """
@@ -29,12 +29,9 @@ def nvcc() -> str:
     raise RuntimeError("nvcc not found")
 
 
-def _flags(debug: bool) -> list[str]:
-    f = ARCH + ["-std=c++17", "-O3", "-lineinfo", "-Xcompiler", "-fPIC,-O3",
-                "--expt-relaxed-constexpr", "-I", INCLUDE, "-I", CSRC]
-    if debug:
-        f += ["-DHA_DEBUG=1"]
-    return f
+def _flags() -> list[str]:
+    return ARCH + ["-std=c++17", "-O3", "-lineinfo", "-Xcompiler", "-fPIC,-O3",
+                   "--expt-relaxed-constexpr", "-I", INCLUDE, "-I", CSRC]
 
 
 def _deps_newer(target: str, deps: list[str]) -> bool:
@@ -44,7 +41,7 @@ def _deps_newer(target: str, deps: list[str]) -> bool:
     return any(os.path.getmtime(d) > t for d in deps)
 
 
-def build(force: bool = False, debug: bool = False, verbose: bool = False) -> str:
+def build(force: bool = False, verbose: bool = False) -> str:
     os.makedirs(OBJDIR, exist_ok=True)
     sources = sorted(f for f in os.listdir(CSRC) if f.endswith(".cu"))
     headers = [os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith((".h", ".cuh"))]
@@ -56,7 +53,7 @@ def build(force: bool = False, debug: bool = False, verbose: bool = False) -> st
         o = os.path.join(OBJDIR, src[:-3] + ".o")
         objs.append(o)
         if force or _deps_newer(o, [s] + headers + [os.path.abspath(__file__)]):
-            jobs.append([nvcc()] + _flags(debug) + ["-c", s, "-o", o])
+            jobs.append([nvcc()] + _flags() + ["-c", s, "-o", o])
 
     def run(cmd):
         r = subprocess.run(cmd, capture_output=True, text=True)
@@ -81,7 +78,6 @@ def build(force: bool = False, debug: bool = False, verbose: bool = False) -> st
 if __name__ == "__main__":
     ap = argparse.ArgumentParser()
     ap.add_argument("--force", action="store_true")
-    ap.add_argument("--debug", action="store_true")
     ap.add_argument("-v", "--verbose", action="store_true")
     a = ap.parse_args()
-    print(build(force=a.force, debug=a.debug, verbose=a.verbose))
+    print(build(force=a.force, verbose=a.verbose))
