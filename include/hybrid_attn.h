@@ -226,9 +226,18 @@ ha_status ha_workspace_size(const ha_params* p, int32_t op, int32_t Tq, int32_t 
 
 /* First error code recorded on the current device by a tensor-core kernel whose
  * pipeline wait ran out of time (0 = none); such a kernel returns early instead
- * of hanging and its outputs are incomplete.  Blocks until the device's prior
- * work is done.  `clear` != 0 resets the code. */
+ * of hanging and its outputs are incomplete.  While a code is set, a wait of a
+ * later tensor-core kernel that would block gives up at once, so the outputs of
+ * later calls are incomplete too until the code is cleared.  Blocks until the
+ * device's prior work is done.  `clear` != 0 resets the code. */
 ha_status ha_device_error(int32_t* code, int32_t clear);
+
+/* Test of the error path above without a fault: launches on `stream` one CTA
+ * that waits on a barrier nothing arrives at, through the same bounded wait as
+ * the tensor-core pipelines; after the wait limit (2 s) it records `code` (> 0)
+ * in the device error word, unless a code is already set, and returns.  Not part
+ * of the method; the device stays usable.  HA_ERR_INVALID_ARG for code <= 0. */
+ha_status ha_selftest_wait_timeout(int32_t code, ha_stream_t stream);
 
 /* Static description of a status code. */
 const char* ha_status_string(ha_status s);

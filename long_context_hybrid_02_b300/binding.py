@@ -56,6 +56,7 @@ _SIGS = {
                                   _P, _P],
     "ha_workspace_size": [ctypes.POINTER(Params), _I, _I, _I, _I, ctypes.POINTER(ctypes.c_size_t)],
     "ha_device_error": [ctypes.POINTER(ctypes.c_int32), _I],
+    "ha_selftest_wait_timeout": [_I, _P],
 }
 EXPORTS = list(_SIGS) + ["ha_status_string", "ha_last_error", "ha_abi_version", "ha_launch_count"]
 
@@ -191,3 +192,9 @@ def ha_device_error(clear: bool = True) -> int:
     code = ctypes.c_int32(0)
     _call("ha_device_error", ctypes.byref(code), int(clear))
     return code.value
+
+
+def ha_selftest_wait_timeout(code: int, stream=None):
+    """Launch the wait-timeout self-test: after the 2 s wait limit the device error
+    word holds `code` (unless a code was already set)."""
+    _call("ha_selftest_wait_timeout", code, _stream(stream))

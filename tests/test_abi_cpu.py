@@ -155,3 +155,10 @@ def _load_fresh(path):
         return B.load_library(path)
     finally:
         B._lib = saved
+
+
+def test_wait_timeout_selftest_checks_its_code_on_the_host(lib):
+    # rejected before any CUDA call: runs without a GPU
+    assert code_of(B.ha_selftest_wait_timeout, 0, 0) == 1
+    assert code_of(B.ha_selftest_wait_timeout, -5, 0) == 1
+    assert "positive" in B.load_library().ha_last_error().decode()
