@@ -50,7 +50,7 @@ def _run():
     t0 = time.perf_counter()
     B.ha_selftest_wait_timeout(78)
     torch.cuda.synchronize()
-    assert time.perf_counter() - t0 < 1.0
+    assert time.perf_counter() - t0 < 1.5          # well under the 2 s limit
     assert B.ha_device_error(clear=True) == 77
     assert B.ha_device_error(clear=False) == 0
     _topk_still_matches_the_oracle()
