@@ -8,6 +8,8 @@
 #include <atomic>
 #include <mutex>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include "common.cuh"
 #include "hybrid_attn.h"
 #include "kernels.h"
@@ -56,6 +58,15 @@ unsigned long long launch_count() { return g_launches.load(); }
 namespace {
 
 thread_local char g_last_error[512] = "";
+
+// One NVTX range per library call (host side: argument checks, planning and the
+// launches), named after the entry point; a no-op unless a profiler is attached.
+struct CallRange {
+  explicit CallRange(const char* name) { nvtxRangePushA(name); }
+  ~CallRange() { nvtxRangePop(); }
+  CallRange(const CallRange&) = delete;
+  CallRange& operator=(const CallRange&) = delete;
+};
 
 ha_status fail(ha_status s, const char* fmt, ...) {
   va_list ap;
@@ -202,6 +213,7 @@ ha_status hca_compress_kv(const ha_params* p, const void* k_tok, const void* v_t
                           int32_t n_blk, void* ck, void* cv, int32_t n_cap,
                           ha_stream_t stream) {
   g_last_error[0] = 0;
+  CallRange range("hca_compress_kv");
   if (!p) return fail(HA_ERR_INVALID_ARG, "params is NULL");
   const void* src[2] = {k_tok, v_tok};
   void* dst[2] = {ck, cv};
@@ -215,6 +227,7 @@ ha_status csa_compress_kv(const ha_params* p, const void* k_tok, const void* v_t
                           const int32_t* blk_begin, int32_t n_blk, void* ck, void* cv,
                           void* cki, int32_t n_cap, ha_stream_t stream) {
   g_last_error[0] = 0;
+  CallRange range("csa_compress_kv");
   if (!p) return fail(HA_ERR_INVALID_ARG, "params is NULL");
   const void* src[3] = {k_tok, v_tok, ki_tok};
   void* dst[3] = {ck, cv, cki};
@@ -227,6 +240,7 @@ ha_status csa_index_scores(const ha_params* p, const void* q_idx, const float* w
                            const void* cki, int32_t n_cap, const int32_t* q_pos, int32_t Tq,
                            float* scores, ha_stream_t stream) {
   g_last_error[0] = 0;
+  CallRange range("csa_index_scores");
   ha_status s = check_params(p, false, true);
   if (s != HA_OK) return s;
   HA_PTR(q_idx);
@@ -252,6 +266,7 @@ ha_status csa_index_scores(const ha_params* p, const void* q_idx, const float* w
 ha_status csa_topk(const ha_params* p, const float* scores, int32_t n_cap, const int32_t* q_pos,
                    int32_t Tq, int32_t* idx, void* ws, size_t ws_bytes, ha_stream_t stream) {
   g_last_error[0] = 0;
+  CallRange range("csa_topk");
   ha_status s = check_params(p, false, false);
   if (s != HA_OK) return s;
   s = check_k(p);
@@ -279,6 +294,7 @@ ha_status hybrid_attn_decode(const ha_params* p, const void* q, const void* ck, 
                              void* o, float* lse, void* ws, size_t ws_bytes,
                              ha_stream_t stream) {
   g_last_error[0] = 0;
+  CallRange range("hybrid_attn_decode");
   ha_status s = check_params(p, true, false);
   if (s != HA_OK) return s;
   if (idx) {
@@ -321,6 +337,7 @@ ha_status hybrid_attn_prefill(const ha_params* p, const void* q, const int32_t* 
                               int32_t tok_cap, void* o, float* lse, void* ws, size_t ws_bytes,
                               ha_stream_t stream) {
   g_last_error[0] = 0;
+  CallRange range("hybrid_attn_prefill");
   ha_status s = check_params(p, true, false);
   if (s != HA_OK) return s;
   if (idx) {
