@@ -155,6 +155,21 @@ def max_over_ranks(value: float, dev, dist, world: int) -> float:
 
 
 NOMINAL_HBM_GBS = 7700.0       # B300 HBM3e, nominal
+L2_FLUSHED = "flushed before every timed step (256 MiB write, then 256 MiB read)"
+GRAPH_TIMING = "CUDA events at both ends of a CUDA graph of the step, per step"
+
+
+def workload_config(w, l2: str, timing: str) -> dict:
+    """The `config` of a JSON line: the workload's sizes (the same keys in both
+    arms) and how the line was timed."""
+    csa = w.kind == "csa"
+    cfg = {"workload": w.name, "kind": w.kind, "B": w.B, "ctx": w.L}
+    if not w.decode:
+        cfg["Tq"] = w.Tq
+    cfg.update({"H": w.H, "d": w.d, "n_win": w.n_win, "m": w.m, "k": w.k if csa else None,
+                "H_I": w.H_I if csa else None, "d_I": w.d_I if csa else None,
+                "l2": l2, "timing": timing})
+    return cfg
 
 
 def peaks():
@@ -265,11 +280,20 @@ def host_inputs(w, seqs: int):
     return synth.make_tokens(ws, "cpu"), synth.make_queries(ws, "cpu")
 
 
+def scaled_workload(w, args):
+    """The workload with the --batch / --ctx overrides applied (both arms)."""
+    if args.batch > 0:
+        w = w.scaled(B=args.batch)
+    if args.ctx > 0:
+        w = w.scaled(L=args.ctx)
+    return w
+
+
 def run_reference(args, rank):
     if rank != 0:
         return
     from long_context_hybrid_02_b300 import synth
-    w = synth.WORKLOADS[args.workload]
+    w = scaled_workload(synth.WORKLOADS[args.workload], args)
     tok, qry = host_inputs(w, 1)
     per_step = max(0.5, min(5.0, 120.0 / max(1, args.steps + args.warmup)))
 
@@ -296,12 +320,14 @@ def run_reference(args, rank):
             "warmup": args.warmup, "ms_per_step": 1e3 * el / max(1, done),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic (seeded Gaussian, host-drawn)",
-            "config": {"workload": w.name, "B": w.B, "ctx": w.L, "H": w.H, "d": w.d,
-                       "n_win": w.n_win, "m": w.m, "k": w.k if w.kind == "csa" else None},
+            "config": workload_config(w, "not applicable (host CPU)",
+                                      "wall clock of the oracle on the host, per step"),
             "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": threads, "kind": "oracle",
                              "host_cpus": cores,
-                             "sample": f"sequence 0 of the workload decoded repeatedly, "
-                                       f"{per_step:.1f}s per step"},
+                             "sample": (f"sequence 0 of the workload decoded repeatedly, "
+                                        f"{per_step:.1f}s per step" if w.decode else
+                                        f"prefill queries of sequence 0, one after the other "
+                                        f"from the end of the chunk, {per_step:.1f}s per step")},
             "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
@@ -515,10 +541,7 @@ def run_prefill(args, w, dev, world, rank, dist):
         "warmup": args.warmup, "ms_per_step": round(step_ms, 5), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded Gaussian drawn on the device)",
-        "config": {"workload": w.name, "kind": w.kind, "B": w.B, "ctx": w.L, "Tq": w.Tq, "H": w.H,
-                   "d": w.d, "n_win": w.n_win, "m": w.m, "k": w.k, "H_I": w.H_I, "d_I": w.d_I,
-                   "l2": "flushed before every timed step (256 MiB write, then 256 MiB read)",
-                   "timing": "CUDA events at both ends of a CUDA graph of the step, per step"},
+        "config": workload_config(w, L2_FLUSHED, GRAPH_TIMING),
         "clocks": clocks.summary(),
         "e2e": {"value": round(e2e_value, 1), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h,
@@ -569,11 +592,7 @@ def main():
     if not os.path.exists(bld.LIB):
         bld.build()
     B.load_library()
-    w = synth.WORKLOADS[args.workload]
-    if args.batch > 0:
-        w = w.scaled(B=args.batch)
-    if args.ctx > 0:
-        w = w.scaled(L=args.ctx)
+    w = scaled_workload(synth.WORKLOADS[args.workload], args)
     if not w.decode:
         return run_prefill(args, w, dev, world, rank, dist)
     tok = synth.make_tokens(w, dev)
@@ -819,12 +838,7 @@ def main():
         "warmup": args.warmup, "ms_per_step": round(step_ms, 5), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if w.dtype == "bf16" else "f32",
         "data": "synthetic (seeded Gaussian drawn on the device)",
-        "config": {"workload": w.name, "kind": w.kind, "B": w.B, "ctx": w.L, "H": w.H, "d": w.d,
-                   "n_win": w.n_win, "m": w.m, "k": w.k if w.kind == "csa" else None,
-                   "H_I": w.H_I if w.kind == "csa" else None,
-                   "d_I": w.d_I if w.kind == "csa" else None,
-                   "l2": "flushed before every timed step (256 MiB write, then 256 MiB read)",
-                   "timing": "CUDA events at both ends of a CUDA graph of the step, per step"},
+        "config": workload_config(w, L2_FLUSHED, GRAPH_TIMING),
         "clocks": clk,
         "e2e": {"value": round(e2e_value, 1), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h,
