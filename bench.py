@@ -364,9 +364,9 @@ def oracle_prefill_sample(w, tok_h, qry_h, seconds: float):
 
 
 def run_prefill(args, w, dev, world, rank, dist):
-    """One prefill chunk of Tq queries per sequence: index every eligible entry for
-    every query (tensor-core GEMM), top-k per query, attention per query over its
-    selection and causal window."""
+    """One prefill chunk of Tq queries per sequence: compress the blocks the chunk's
+    tokens complete, index every eligible entry for every query (tensor-core GEMM),
+    top-k per query, attention per query over its selection and causal window."""
     import torch
     from long_context_hybrid_02_b300 import binding as B
     from long_context_hybrid_02_b300 import synth
@@ -375,25 +375,33 @@ def run_prefill(args, w, dev, world, rank, dist):
     qry = synth.make_queries(w, dev)
     layer = HybridLayer(w, tok, dev)
     layer.build_cache()
+    # the chunk's tokens are positions L0 .. L-1: the blocks they complete are
+    # compressed inside every step (rewriting the same entries each time)
+    L0 = w.L - w.Tq
+    blk0, n_blk_chunk = L0 // w.m, w.L // w.m - L0 // w.m
+    blk_chunk = torch.full((w.B,), blk0, dtype=torch.int32, device=dev)
     stream = torch.cuda.Stream(device=dev)
-    names = ["index", "topk", "attention"]
-    ev = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(4)]
+    names = ["compress", "index", "topk", "attention"]
+    ev = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(len(names) + 1)]
     ws = (layer.ws.data_ptr(), layer.ws.numel())
 
     def step(marks: bool):
         s = stream.cuda_stream
         ev[0].record(stream)
+        layer.compress(blk_chunk, n_blk_chunk, s)
+        if marks:
+            ev[1].record(stream)
         B.csa_index_scores(layer.p, qry["qI"], qry["w_idx"], layer.cki, layer.n_cap, qry["q_pos"],
                            w.Tq, layer.scores, s)
         if marks:
-            ev[1].record(stream)
+            ev[2].record(stream)
         B.csa_topk(layer.p, layer.scores, layer.n_cap, qry["q_pos"], w.Tq, layer.idx, ws, s)
         if marks:
-            ev[2].record(stream)
+            ev[3].record(stream)
         B.hybrid_attn_prefill(layer.p, qry["q"], qry["q_pos"], w.Tq, layer.ck, layer.cv,
                               layer.n_cap, layer.idx, tok["k_tok"], tok["v_tok"], layer.tok_cap,
                               layer.o, layer.lse, ws, s)
-        ev[3].record(stream)
+        ev[4].record(stream)
 
     with torch.cuda.stream(stream):
         step(True)
@@ -417,9 +425,9 @@ def run_prefill(args, w, dev, world, rank, dist):
             torch.sum(flush_r, dim=0, out=flush_out)
             g.replay()
             torch.cuda.synchronize()
-            tot.append(ev[0].elapsed_time(ev[3]))
+            tot.append(ev[0].elapsed_time(ev[len(names)]))
             if g is graphs[True]:
-                per.append([ev[j].elapsed_time(ev[j + 1]) for j in range(3)])
+                per.append([ev[j].elapsed_time(ev[j + 1]) for j in range(len(names))])
         return tot, per
 
     for _ in range(args.warmup):
@@ -456,10 +464,14 @@ def run_prefill(args, w, dev, world, rank, dist):
                 "algorithmic_flops": attn_flops,
                 "peak_source": pk["source"] + " (MEASURED_PEAKS.json bf16_tflops, burst)"}
 
-    # end to end: the chunk's queries from pinned host memory, outputs back
+    # end to end: the chunk's token rows and queries from pinned host memory, outputs back
     h_in = {k: torch.empty_like(qry[k], device="cpu").pin_memory() for k in ("q", "qI", "w_idx")}
     for k in h_in:
         h_in[k].copy_(qry[k])
+    tok_names = ("k_tok", "v_tok", "ki_tok", "gate")
+    for k in tok_names:
+        h_in["chunk_" + k] = torch.empty_like(tok[k][:, L0:w.L], device="cpu").pin_memory()
+        h_in["chunk_" + k].copy_(tok[k][:, L0:w.L])
     h_out = torch.empty_like(layer.o, device="cpu").pin_memory()
     h2d = sum(x.numel() * x.element_size() for x in h_in.values())
     d2h = h_out.numel() * h_out.element_size()
@@ -487,6 +499,9 @@ def run_prefill(args, w, dev, world, rank, dist):
                 qry["q"][:, c * sub:(c + 1) * sub].copy_(h_in["q"][:, c * sub:(c + 1) * sub],
                                                          non_blocking=True)
                 q_ready[c].record(qside)
+        for k in tok_names:
+            tok[k][:, L0:w.L].copy_(h_in["chunk_" + k], non_blocking=True)
+        layer.compress(blk_chunk, n_blk_chunk, s)
         for k in ("qI", "w_idx"):
             qry[k].copy_(h_in[k], non_blocking=True)
         B.csa_index_scores(layer.p, qry["qI"], qry["w_idx"], layer.cki, layer.n_cap, qry["q_pos"],
@@ -545,10 +560,12 @@ def run_prefill(args, w, dev, world, rank, dist):
         "clocks": clocks.summary(),
         "e2e": {"value": round(e2e_value, 1), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h,
-                "timing": "per step: pinned-host copies of the chunk's inputs, the step and the "
-                          "copy of o back, one graph between CUDA events; q copied beside "
-                          "scoring and selection, attention in 4 sub-chunks of queries whose "
-                          "outputs are copied back beside the next; L2 flushed before every step"},
+                "timing": "per step: pinned-host copies of the chunk's token rows (K, V, indexer "
+                          "keys, gates) and queries, the step (compression of the blocks the "
+                          "chunk completes first) and the copy of o back, one graph between "
+                          "CUDA events; q copied beside compression, scoring and selection, "
+                          "attention in 4 sub-chunks of queries whose outputs are copied back "
+                          "beside the next; L2 flushed before every step"},
         "gpu_launches": int(launches_per_step) * args.steps,
         "roofline": roofline,
         "indexer_tflops": round(idx_tf, 1),
