@@ -64,3 +64,79 @@ def test_reference_arm_under_torchrun_prints_on_rank_0_only():
     assert r.returncode == 0, r.stderr[-2000:]
     lines = _json_lines(r.stdout)
     assert len(lines) == 1 and lines[0]["n_gpus"] == 2 and lines[0]["impl"] == "reference"
+
+
+def _bench():
+    sys.path.insert(0, ROOT)
+    import bench
+    return bench
+
+
+def test_algorithmic_bytes_of_the_64k_csa_step():
+    # worked by hand: per row (512 + 128) keys x (K + V) x 512 dims x 2 B, q and o
+    # 64 x 512 x 2 B each, 512 int32 indices; per indexer row 16,352 entries x 128
+    # x 2 B keys + 16,352 x 4 B scores + 64 x 128 x 2 B q + 64 x 4 B weights
+    bench = _bench()
+    from long_context_hybrid_02_b300 import synth
+    w = synth.WORKLOADS["csa_decode_64k"]
+    ne = (w.L - w.n_win) // w.m
+    assert ne == 16352
+    nb = bench.step_bytes(w, ne, w.n_win)
+    assert nb["attention"] == 32 * (640 * 2 * 512 * 2 + 2 * 64 * 512 * 2 + 512 * 4) == 46202880
+    assert nb["index"] == 32 * (16352 * 256 + 16352 * 4 + 64 * 256 + 64 * 4) == 136581120
+    assert nb["topk"] == 32 * (16352 * 4 + 512 * 4)
+
+
+def test_traffic_row_applies_only_to_its_workload_kernel_and_source(tmp_path, monkeypatch):
+    import hashlib
+    bench = _bench()
+    src = tmp_path / "long_context_hybrid_02_b300" / "csrc"
+    src.mkdir(parents=True)
+    (src / "k.cu").write_text("kernel v1\n")
+    sha = hashlib.sha256(b"kernel v1\n").hexdigest()[:16]
+    (tmp_path / "profiles").mkdir()
+    (tmp_path / "profiles" / "dram_traffic.md").write_text(
+        "| workload | kernel key | source | bytes per launch | source sha256[:16] | note |\n"
+        "|---|---|---|---|---|---|\n"
+        f"| wl_a | attention | k.cu | 12345 | {sha} | x |\n")
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    assert bench.profiled_traffic("wl_a", "attention", "k.cu") == 12345.0
+    assert bench.profiled_traffic("wl_b", "attention", "k.cu") is None
+    assert bench.profiled_traffic("wl_a", "index", "k.cu") is None
+    assert bench.profiled_traffic(None, "attention", "k.cu") is None       # not full size
+    (src / "k.cu").write_text("kernel v2\n")                                # source changed
+    assert bench.profiled_traffic("wl_a", "attention", "k.cu") is None
+
+
+def test_clock_summary_from_a_fake_nvml(monkeypatch):
+    import time
+    bench = _bench()
+    cs = bench.ClockSampler(None)
+    clocks = iter([2032, 1900, 2032, 2032] + [2032] * 10000)
+    monkeypatch.setattr(cs, "_open_nvml",
+                        lambda: (lambda: next(clocks), lambda: 2032, lambda: 0x4 | 0x1))
+    with cs:
+        time.sleep(0.05)
+    s = cs.summary()
+    assert s["sm_mhz"] == 2032 and s["sm_max_mhz"] == 2032 and s["samples"] >= 4
+    assert s["reasons"] == ["sw_power_cap"]                # 0x1 (idle) is not reported
+
+
+def test_clock_summary_names_a_throttle_and_a_missing_nvml(monkeypatch):
+    import time
+    bench = _bench()
+    cs = bench.ClockSampler(None)
+    monkeypatch.setattr(cs, "_open_nvml",
+                        lambda: (lambda: 1500, lambda: 2032, lambda: 0x8 | 0x40))
+    with cs:
+        time.sleep(0.02)
+    assert cs.summary()["reasons"] == ["hw_slowdown", "hw_thermal_slowdown"]
+
+    def no_nvml():
+        raise OSError("libnvidia-ml.so.1: cannot open shared object file")
+    cs2 = bench.ClockSampler(None)
+    monkeypatch.setattr(cs2, "_open_nvml", no_nvml)
+    with cs2:
+        pass
+    s = cs2.summary()
+    assert s["sm_mhz"] is None and s["reasons"][0].startswith("nvml unavailable")
