@@ -55,6 +55,7 @@ import numpy as np
 
 __all__ = [
     "round_to_bf16", "round_to_storage", "round_to_e4m3", "fp8_kv_encode", "fp8_kv_decode",
+    "round_to_e2m1", "fp4_encode", "fp4_decode",
     "gate_softmax", "compress_block",
     "compress", "n_eligible", "window_positions", "index_scores", "topk_select",
     "attend", "merge_partials", "csa_decode", "hca_decode", "prefill_query",
@@ -137,6 +138,53 @@ def fp8_kv_decode(rope, codes, scale):
     """The row a FP8-format entry stands for (float64): RoPE dims, then code * scale."""
     return np.concatenate([np.asarray(rope, np.float64),
                            (np.asarray(codes, np.float64) * np.asarray(scale, np.float64)[:, None]).reshape(-1)])
+
+
+# --------------------------------------------------------------------------
+# the indexer in FP4 ([V4-notes] §8: the lightning indexer's attention
+# computation runs in FP4, and its index scores are kept as BF16).  The page
+# names the precision, not the layout; the reading used here: a row of indexer
+# queries or keys is cut into groups of 16 consecutive elements, each element an
+# e2m1 value (sign, 2 exponent bits, 1 mantissa bit: magnitudes 0, 0.5, 1, 1.5, 2,
+# 3, 4, 6) with one e4m3 scale per group, scale = max|x| / 6 rounded to e4m3,
+# codes rounded to nearest, ties to even, magnitudes above 6 saturating to 6.
+# --------------------------------------------------------------------------
+E2M1_MAX = 6.0
+FP4_GROUP = 16
+
+
+def round_to_e2m1(x):
+    """Nearest e2m1 value (ties to the even mantissa), saturating at +-6; NaN stays NaN.
+
+    Below 2 the values are 0.5 apart, in [2, 4) 1 apart, from 4 on 2 apart.
+    """
+    x = np.asarray(x, dtype=np.float64)
+    a = np.abs(x)
+    _, expo = np.frexp(a)                          # a = f * 2**expo, f in [0.5, 1)
+    e = np.maximum(expo - 1, 0)                    # binade of a (0 for a < 2)
+    step = np.ldexp(1.0, e - 1)
+    q = np.minimum(np.rint(a / step) * step, E2M1_MAX)   # rint: ties to even
+    q = np.where(np.isnan(x), np.nan, q)
+    return np.copysign(q, x)
+
+
+def fp4_encode(rows):
+    """Rows [n, d] (d a multiple of 16) -> (codes [n, d/16, 16] e2m1 values,
+    scales [n, d/16] e4m3 values); an all-zero group gets scale 0 and codes 0."""
+    rows = np.asarray(rows, dtype=np.float64)
+    n, d = rows.shape
+    g = rows.reshape(n, d // FP4_GROUP, FP4_GROUP)
+    scale = round_to_e4m3(np.abs(g).max(axis=-1) / E2M1_MAX)
+    safe = np.where(scale > 0, scale, 1.0)
+    codes = np.where(scale[..., None] > 0, round_to_e2m1(g / safe[..., None]), 0.0)
+    return codes, scale
+
+
+def fp4_decode(codes, scale):
+    """Inverse of fp4_encode: rows [n, d] = codes * scale of their group."""
+    codes = np.asarray(codes, dtype=np.float64)
+    scale = np.asarray(scale, dtype=np.float64)
+    return (codes * scale[..., None]).reshape(codes.shape[0], -1)
 
 
 # --------------------------------------------------------------------------
