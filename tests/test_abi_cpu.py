@@ -1,7 +1,6 @@
 """The C-ABI library loads, exports every entry point of include/hybrid_attn.h and
 rejects bad arguments on the host (no GPU needed: validation runs before any
 CUDA call)."""
-import ctypes
 import os
 import re
 
