@@ -73,6 +73,22 @@ def test_fp4_rows_error_bound(seed):
     assert (np.abs(dtop - top) <= 2.0 ** -4 * np.abs(top) * (1 + 2.0 ** -20)).all()
 
 
+def test_pins_catch_ties_rounded_away_from_zero(monkeypatch):
+    good = O.round_to_e2m1
+
+    def away(x):
+        x = np.asarray(x, dtype=np.float64)
+        a = np.abs(x)
+        _, expo = np.frexp(a)
+        step = np.ldexp(1.0, np.maximum(expo - 1, 0) - 1)
+        return np.copysign(np.minimum(np.floor(a / step + 0.5) * step, 6.0), x)
+
+    monkeypatch.setattr(O, "round_to_e2m1", away)
+    with pytest.raises(AssertionError):
+        test_e2m1_midpoints_round_to_even_mantissa()
+    assert good(2.5) == 2.0 and away(2.5) == 3.0
+
+
 # ----------------------------------------------------------------- diagnostic
 H_I, D_I = 64, 128
 

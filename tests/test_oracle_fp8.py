@@ -112,3 +112,11 @@ def test_diagnostic_attention_over_fp8_rows():
     rel_o = np.linalg.norm(o8 - o) / np.linalg.norm(o)
     print(f"fp8 rows {rel_rows:.4f}, o {rel_o:.4f}, max lse shift {np.abs(lse8 - lse).max():.2e}")
     assert 0.01 < rel_rows < 0.04 and rel_o < 0.04 and np.abs(lse8 - lse).max() < 1e-3
+
+
+def test_pins_catch_a_scale_for_the_wrong_e4m3_variant(monkeypatch):
+    # 240 is the largest finite value of the "fnuz" e4m3 variant, not of e4m3fn
+    import oracle.hybrid_attention as H
+    monkeypatch.setattr(H, "E4M3_MAX", 240.0)
+    with pytest.raises(AssertionError):
+        test_fp8_kv_constant_row()

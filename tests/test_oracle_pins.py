@@ -380,6 +380,71 @@ def test_pins_catch_a_dropped_relu(monkeypatch):
         test_index_scores_worked_example()
 
 
+def test_pins_catch_a_squared_softmax_scale(monkeypatch):
+    good = O.attend
+    monkeypatch.setattr(O, "attend", lambda q, k, v, scale: good(q, k, v, scale * scale))
+    with pytest.raises(AssertionError):
+        test_attend_matches_textbook_sdpa()
+
+
+def _bad_topk(larger_index_first: bool, sort_output: bool):
+    def topk(scores, k):
+        s = np.asarray(scores, dtype=np.float64).copy()
+        s[np.isnan(s)] = -np.inf
+        n = s.shape[0]
+        tie = -np.arange(n) if larger_index_first else np.arange(n)
+        order = np.lexsort((tie, -s))[:min(k, n)]
+        out = np.full(k, -1, dtype=np.int64)
+        out[:order.size] = np.sort(order) if sort_output else order
+        return out
+    return topk
+
+
+def test_pins_catch_ties_broken_toward_the_larger_index(monkeypatch):
+    monkeypatch.setattr(O, "topk_select", _bad_topk(larger_index_first=True, sort_output=True))
+    with pytest.raises(AssertionError):
+        test_topk_matches_heap_selection_with_ties_and_nan()
+
+
+def test_pins_catch_a_selection_left_in_score_order(monkeypatch):
+    monkeypatch.setattr(O, "topk_select", _bad_topk(larger_index_first=False, sort_output=False))
+    with pytest.raises(AssertionError):
+        test_topk_matches_heap_selection_with_ties_and_nan()
+
+
+def test_pins_catch_a_merge_that_ignores_the_lse_weights(monkeypatch):
+    monkeypatch.setattr(O, "merge_partials", lambda o, lse: (np.asarray(o).mean(axis=0),
+                                                              np.asarray(lse).max(axis=0)))
+    with pytest.raises(AssertionError):
+        test_merge_partials_equals_joint_attention()
+
+
+def test_pins_catch_separate_softmaxes_for_window_and_entries(monkeypatch):
+    good_attend, good_ne = O.attend, O.n_eligible
+
+    def two_softmaxes(q, ck, cv, k_tok, v_tok, t, *, n_win, m, scale, rule="disjoint"):
+        ne = good_ne(t, n_win, m, rule)
+        win = O.window_positions(t, n_win)
+        ow, lw = good_attend(q, k_tok[win], v_tok[win], scale)
+        if ne == 0:
+            return ow, lw
+        oc, lc = good_attend(q, ck[:ne], cv[:ne], scale)
+        return (ow + oc) / 2, np.logaddexp(lw, lc)
+
+    monkeypatch.setattr(O, "hca_decode", two_softmaxes)
+    with pytest.raises(AssertionError):
+        test_layer_with_blockwise_constant_kv_is_attention_over_block_rows("hca", 128, 1023)
+
+
+def test_pins_catch_bf16_by_truncation(monkeypatch):
+    def truncate(x):
+        a = np.ascontiguousarray(np.asarray(x, dtype=np.float32))
+        return (a.view(np.uint32) & np.uint32(0xFFFF0000)).view(np.float32).astype(np.float64)
+    monkeypatch.setattr(O, "round_to_bf16", truncate)
+    with pytest.raises(AssertionError):
+        test_bf16_rounding_ties_and_exact_values()
+
+
 def test_oracle_package_exports():
     for name in O.__all__:
         assert getattr(oracle, name) is getattr(O, name)
