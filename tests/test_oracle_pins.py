@@ -106,6 +106,20 @@ def test_compress_brute_force_tiny():
             assert abs(out[b, c] - ref) < 1e-14
 
 
+def test_compress_rounds_to_the_cache_storage_type():
+    """The compressed cache holds entries in its storage type: the bf16 result is
+    torch's float64 -> bfloat16 cast of the fp64 result (on the bf16 grid), the
+    fp32 result its float32 cast."""
+    rng = np.random.default_rng(14)
+    X, g = rng.standard_normal((64, 40)) / 7, rng.standard_normal(64)
+    exact = O.compress(X, g, 4, 0, 16)
+    for storage, dt in (("bf16", torch.bfloat16), ("f32", torch.float32)):
+        got = O.compress(X, g, 4, 0, 16, storage)
+        ref = torch.tensor(exact, dtype=torch.float64).to(dt).double().numpy()
+        np.testing.assert_array_equal(got, ref)
+    assert not np.array_equal(O.compress(X, g, 4, 0, 16, "bf16"), exact)
+
+
 def test_compress_rejects_incomplete_block():
     with pytest.raises(ValueError):
         O.compress(np.zeros((10, 2)), np.zeros(10), 4, 2, 1)
@@ -443,6 +457,12 @@ def test_pins_catch_bf16_by_truncation(monkeypatch):
     monkeypatch.setattr(O, "round_to_bf16", truncate)
     with pytest.raises(AssertionError):
         test_bf16_rounding_ties_and_exact_values()
+
+
+def test_pins_catch_an_unrounded_cache(monkeypatch):
+    monkeypatch.setattr(O, "round_to_storage", lambda x, storage: np.asarray(x, dtype=np.float64))
+    with pytest.raises(AssertionError):
+        test_compress_rounds_to_the_cache_storage_type()
 
 
 def test_oracle_package_exports():
