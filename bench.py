@@ -12,7 +12,10 @@ captured once in a CUDA graph and replayed; timing uses CUDA events recorded at
 both ends of the graph on the launching stream, with an L2 flush (256 MiB write,
 then 256 MiB read) before every timed step.  The library's kernels are chained
 with programmatic dependent launch, so the per-kernel breakdown comes from a
-second graph with an event between every two calls.
+second graph with an event between every two calls.  Other workloads
+(--workload): HCA decode at 128K tokens, the million-token decodes, and a CSA
+prefill chunk of 4,096 queries (compress the blocks the chunk completes, score,
+select, attend; prefill tokens/s).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
 
