@@ -28,8 +28,11 @@
  *
  * Conventions shared by every call
  *   - Every pointer argument except `p` is DEVICE memory owned by the caller.
- *     The library allocates nothing, keeps no state between calls and never
- *     synchronises the host; all work is ordered on `stream` (0 = legacy default).
+ *     The library allocates nothing and never synchronises the host (except
+ *     ha_device_error, which reads a device word); all work is ordered on
+ *     `stream` (0 = legacy default).  Nothing carries from one call to the next
+ *     but the device error word (ha_device_error) and the fixed scratch of
+ *     hybrid_attn_decode_static.
  *   - Arrays are row-major with the last dimension contiguous.  "T" is the
  *     storage type selected by p->dtype (float for HA_F32, bfloat16 for
  *     HA_BF16).  Gates, indexer weights, scores and lse are always float32;
