@@ -207,9 +207,11 @@ ha_status hybrid_attn_prefill(const ha_params* p, const void* q, const int32_t* 
  * Same arguments, results and checks as hybrid_attn_decode.  The split-KV
  * partials go to a fixed 32 MiB array in device global memory owned by the
  * library; each device that loads the library holds that array until the
- * process exits.  Problems whose partials need more than 32 MiB
- * (ha_workspace_size(p, HA_OP_DECODE, 1, n_cap, idx != NULL)) return
- * HA_ERR_WORKSPACE without launching.  Allocates nothing.
+ * process exits.  Problems whose partials need more than 32 MiB (the workspace
+ * hybrid_attn_decode would need for the same arguments, tok_cap included; this is
+ * ha_workspace_size(p, HA_OP_DECODE, 1, n_cap, idx != NULL) unless B * tok_cap
+ * reaches 2^30) return HA_ERR_WORKSPACE without launching, with a message naming
+ * the static scratch.  Allocates nothing.
  * Every call on a device shares the array and leaves its last contents behind
  * (no part of it needs to start at zero); calls whose kernels overlap on the GPU
  * race on it, so order them on one stream.  The first call on a device looks up

@@ -184,6 +184,10 @@ ha_status compress_common(const ha_params* p, int n_tensors, const void* const* 
 
 }  // namespace
 
+size_t ha::decode_workspace_bytes(const ha_params* p, int n_cap, int tok_cap, bool is_csa) {
+  return attention_plan(p, p->B, n_cap, tok_cap, is_csa, true).ws_bytes;
+}
+
 void ha::set_last_error(const char* msg) {
   snprintf(g_last_error, sizeof(g_last_error), "%s", msg);
 }

@@ -65,9 +65,12 @@ ha_status hybrid_attn_decode_static(const ha_params* p, const void* q, const voi
                                     const void* k_tok, const void* v_tok, int32_t tok_cap,
                                     const int32_t* ctx_len, void* o, float* lse,
                                     ha_stream_t stream) {
+  // ha_workspace_size checks the parameters; the size itself comes from the plan
+  // hybrid_attn_decode makes for these very arguments (tok_cap can change it)
   size_t need = 0;
   ha_status s = ha_workspace_size(p, HA_OP_DECODE, 1, n_cap, idx != nullptr ? 1 : 0, &need);
   if (s != HA_OK) return s;
+  need = ha::decode_workspace_bytes(p, n_cap, tok_cap, idx != nullptr);
   char msg[256];
   if (need > kStaticScratchBytes) {
     snprintf(msg, sizeof(msg),

@@ -12,6 +12,11 @@ namespace ha {
 // api.cu: replace the message returned by ha_last_error() on this thread.
 void set_last_error(const char* msg);
 
+// api.cu: workspace bytes hybrid_attn_decode needs for these arguments (the same
+// plan the call itself makes, tok_cap included); p must have passed the checks of
+// ha_workspace_size.
+size_t decode_workspace_bytes(const ha_params* p, int n_cap, int tok_cap, bool is_csa);
+
 // status.cu: device address of the error word of the tensor-core kernels on the
 // current device (null if it cannot be looked up).
 int* device_error_word();

@@ -44,6 +44,10 @@ of the repository):
   * top-k order: score descending, then smaller index; NaN scores rank as -inf;
     the result is emitted in ascending index order, padded with -1.
   * a query with no key at all (context 0) gives o = 0 and lse = -inf.
+  * a given selection may hold entries that are not eligible: entries < 0 (the
+    -1 padding) or >= min(n_elig(t), n_cap), n_cap = the rows of the compressed
+    cache, are ignored; an entry listed twice is attended twice (the top-k never
+    lists one twice).
   * compressed entries are rounded to the storage type (round-to-nearest-even to
     bfloat16, or to float32) because the cache stores them in that type.
 """
@@ -322,13 +326,19 @@ def merge_partials(o_parts, lse_parts):
     return o, lse
 
 
-def _joint_keys(comp_idx, ck, cv, k_tok, v_tok, t, n_win):
-    win = window_positions(t, n_win)
+def _joint_keys(comp_idx, ck, cv, k_tok, v_tok, t, n_win, tok_base=0):
+    """Key and value rows of one query: the compressed entries comp_idx, then the
+    window positions of t (row u - tok_base of k_tok / v_tok holds position u).
+    Rows are picked first and widened to float64 after (widening is exact)."""
+    win = window_positions(t, n_win) - tok_base
+    if win.size and win[0] < 0:
+        raise ValueError("the per-token rows do not cover the window")
     comp_idx = np.asarray(comp_idx, dtype=np.int64)
-    keys = np.concatenate([np.asarray(ck, np.float64)[comp_idx].reshape(-1, k_tok.shape[1]),
-                           np.asarray(k_tok, np.float64)[win]], axis=0)
-    vals = np.concatenate([np.asarray(cv, np.float64)[comp_idx].reshape(-1, v_tok.shape[1]),
-                           np.asarray(v_tok, np.float64)[win]], axis=0)
+    k_tok, v_tok = np.asarray(k_tok), np.asarray(v_tok)
+    keys = np.concatenate([np.asarray(ck)[comp_idx].reshape(-1, k_tok.shape[1]).astype(np.float64),
+                           k_tok[win].astype(np.float64)], axis=0)
+    vals = np.concatenate([np.asarray(cv)[comp_idx].reshape(-1, v_tok.shape[1]).astype(np.float64),
+                           v_tok[win].astype(np.float64)], axis=0)
     return keys, vals
 
 
@@ -361,17 +371,23 @@ def hca_decode(q, ck, cv, k_tok, v_tok, t: int, *, n_win: int, m: int, scale: fl
 
 
 def prefill_query(q, idx, ck, cv, k_tok, v_tok, t: int, *, n_win: int, m: int, scale: float,
-                  rule: str = "disjoint"):
-    """Attention of one prefill query at position t.
+                  rule: str = "disjoint", tok_base: int = 0):
+    """Attention of one query at position t over a given selection plus its window.
 
-    idx: this query's selected entries (CSA, -1 padded) or None for HCA (all
-    eligible entries).  Positions between the last eligible block and the window
-    start are not attended (the window stays exactly n_win wide).
+    Serves a decode query (t = context length - 1) as well as each query of a
+    prefill chunk.  idx: this query's selected entries (CSA, in any order, -1
+    padded) or None for HCA (all eligible entries).  Entries of idx that are < 0
+    or >= min(n_elig(t), n_cap), n_cap = len(ck), are ignored.  Positions between
+    the last eligible block and the window start are not attended (the window
+    stays exactly n_win wide).  Row r of k_tok / v_tok holds position tok_base + r
+    (0: indexed by absolute position).
     """
+    n_cap = np.asarray(ck).shape[0]
+    ne = min(n_eligible(t, n_win, m, rule), n_cap)
     if idx is None:
-        sel = np.arange(n_eligible(t, n_win, m, rule))
+        sel = np.arange(ne)
     else:
-        idx = np.asarray(idx, dtype=np.int64)
-        sel = idx[idx >= 0]
-    keys, vals = _joint_keys(sel, ck, cv, k_tok, v_tok, t, n_win)
+        idx = np.asarray(idx, dtype=np.int64).reshape(-1)
+        sel = idx[(idx >= 0) & (idx < ne)]
+    keys, vals = _joint_keys(sel, ck, cv, k_tok, v_tok, t, n_win, tok_base)
     return attend(q, keys, vals, scale)

@@ -367,6 +367,46 @@ def test_prefill_query_equals_decode_at_that_position():
         np.testing.assert_allclose(a, b, rtol=1e-14)
 
 
+def _eligible_by_enumeration(t, n_win, m, n_cap):
+    """Entries whose whole block ends before the window of t, listed one by one."""
+    lo = max(0, t - n_win + 1)
+    return [j for j in range(n_cap) if (j + 1) * m - 1 < lo]
+
+
+@pytest.mark.parametrize("t", [0, 130, 131, 300, 599])
+def test_prefill_query_with_a_selection_attends_its_eligible_entries_and_the_window(t):
+    """A query with a given selection (unsorted, -1 padded, with entries beyond the
+    eligible blocks, beyond the cache and listed twice) attends exactly to the
+    listed eligible entries, each as often as listed, plus its window: textbook
+    float64 attention over that key list, with eligibility enumerated here."""
+    rng = np.random.default_rng(600 + t)
+    L, d, H, m, n_win = 600, 16, 3, 4, 128
+    K, V = _tokens(rng, L, d)
+    for n_cap in (L // m, 20):                      # 20 rows: a cache shorter than n_elig
+        ck, cv = _tokens(rng, n_cap, d)
+        elig = _eligible_by_enumeration(t, n_win, m, n_cap)
+        chosen = list(rng.permutation(elig)[:7]) if elig else []
+        if chosen:
+            chosen.append(chosen[0])                # listed twice
+        over = [n_cap - 1 + 5, L // m + 3, 10 ** 6]  # never eligible for this cache
+        if len(elig) < n_cap:
+            over.append(len(elig))                  # first block overlapping the window
+        idx = np.array(chosen + over + [-1, -1, -7], dtype=np.int64)[rng.permutation(len(chosen) + len(over) + 3)]
+        q = rng.standard_normal((H, d))
+        keep = [int(j) for j in idx if int(j) in set(elig)]
+        lo = max(0, t - n_win + 1)
+        keys = np.concatenate([ck[keep].reshape(-1, d), K[lo:t + 1]])
+        vals = np.concatenate([cv[keep].reshape(-1, d), V[lo:t + 1]])
+        o, lse = O.prefill_query(q, idx, ck, cv, K, V, t, n_win=n_win, m=m, scale=d ** -0.5)
+        np.testing.assert_allclose(o, sdpa64(q, keys, vals, d ** -0.5), rtol=1e-12, atol=1e-14)
+        # the same query given only its window's per-token rows (row 0 = position lo)
+        o2, lse2 = O.prefill_query(q, idx, ck, cv, K[lo:t + 1], V[lo:t + 1], t, n_win=n_win, m=m,
+                                   scale=d ** -0.5, tok_base=lo)
+        assert np.array_equal(o, o2) and np.array_equal(lse, lse2)
+        z = (d ** -0.5) * q @ keys.T
+        np.testing.assert_allclose(lse, [math.log(math.fsum(np.exp(r))) for r in z], rtol=1e-13)
+
+
 # ----------------------------------------------------------------- planted mistakes
 def test_pins_catch_an_off_by_one_eligibility(monkeypatch):
     good = O.n_eligible
@@ -463,6 +503,40 @@ def test_pins_catch_an_unrounded_cache(monkeypatch):
     monkeypatch.setattr(O, "round_to_storage", lambda x, storage: np.asarray(x, dtype=np.float64))
     with pytest.raises(AssertionError):
         test_compress_rounds_to_the_cache_storage_type()
+
+
+def _query_with(keep):
+    """prefill_query whose selection filter is `keep(idx, ne, n_cap)` (a planted mistake)."""
+    def prefill_query(q, idx, ck, cv, k_tok, v_tok, t, *, n_win, m, scale, rule="disjoint"):
+        n_cap = np.asarray(ck).shape[0]
+        ne = min(O.n_eligible(t, n_win, m, rule), n_cap)
+        idx = np.asarray(idx, dtype=np.int64)
+        sel = idx[keep(idx, ne, n_cap)]
+        keys = np.concatenate([np.asarray(ck)[sel], np.asarray(k_tok)[O.window_positions(t, n_win)]])
+        vals = np.concatenate([np.asarray(cv)[sel], np.asarray(v_tok)[O.window_positions(t, n_win)]])
+        return O.attend(q, keys, vals, scale)
+    return prefill_query
+
+
+def test_pins_catch_a_selection_whose_padding_is_not_filtered(monkeypatch):
+    # -1 kept: numpy reads it as the cache's last row
+    monkeypatch.setattr(O, "prefill_query", _query_with(lambda i, ne, n: (i < ne)))
+    with pytest.raises(AssertionError):
+        test_prefill_query_with_a_selection_attends_its_eligible_entries_and_the_window(300)
+
+
+def test_pins_catch_a_selection_that_keeps_ineligible_entries(monkeypatch):
+    monkeypatch.setattr(O, "prefill_query", _query_with(lambda i, ne, n: (i >= 0) & (i < n)))
+    with pytest.raises(AssertionError):
+        test_prefill_query_with_a_selection_attends_its_eligible_entries_and_the_window(300)
+
+
+def test_pins_catch_a_selection_that_drops_repeated_entries(monkeypatch):
+    monkeypatch.setattr(O, "prefill_query", _query_with(
+        lambda i, ne, n: ((i >= 0) & (i < ne)) & (np.unique(i, return_index=True)[1][
+            np.searchsorted(np.unique(i), i)] == np.arange(i.size))))
+    with pytest.raises(AssertionError):
+        test_prefill_query_with_a_selection_attends_its_eligible_entries_and_the_window(300)
 
 
 def test_oracle_package_exports():

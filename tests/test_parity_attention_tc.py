@@ -17,7 +17,7 @@ import torch
 import oracle as O
 from long_context_hybrid_02_b300 import binding as B
 from long_context_hybrid_02_b300 import synth
-from tests._harness import assert_close, np64
+from tests._harness import assert_close, assert_lse_close, np64
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
@@ -47,18 +47,19 @@ def _decode(p, q, ck, cv, n_cap, idx, k_tok, v_tok, tok_cap, ctx):
     return o, lse
 
 
-def _check_row(o, lse, q, sel, ck, cv, K, V, t, n_win, scale, what):
-    """o/lse of one query row against the oracle over `sel` + the window of t."""
+def _check_row(o, lse, q, idx, ck, cv, K, V, t, n_win, m, scale, what, rule="disjoint"):
+    """o/lse of one query row against the oracle: the row's raw index set (None:
+    every eligible entry) + the window of t; the oracle ignores -1 and ineligible
+    entries itself."""
     if t < 0:
         assert (np64(o) == 0).all(), what
         assert np.isneginf(np64(lse)).all(), what
         return
-    win = O.window_positions(t, n_win)
-    keys = np.concatenate([ck[sel], K[win]])
-    vals = np.concatenate([cv[sel], V[win]])
-    ro, rl = O.attend(q, keys, vals, scale)
+    if idx is not None:
+        idx = np.asarray(idx.cpu() if torch.is_tensor(idx) else idx, dtype=np.int64)
+    ro, rl = O.prefill_query(q, idx, ck, cv, K, V, t, n_win=n_win, m=m, scale=scale, rule=rule)
     assert_close(np64(o), ro, "bf16", what + " o")
-    assert_close(np64(lse), rl, "bf16", what + " lse")
+    assert_lse_close(np64(lse), rl, "bf16", what + " lse")
 
 
 def test_tc_decode_csa_ragged_contexts_and_index_sets():
@@ -80,9 +81,8 @@ def test_tc_decode_csa_ragged_contexts_and_index_sets():
     o, lse = _decode(p, q, ck, cv, n_cap, idx.to(DEV), k_tok, v_tok, L, ctx_t)
     CK, CV = np64(ck), np64(cv)
     for b, c in enumerate(ctx):
-        sel = [int(j) for j in idx[b] if 0 <= j < ne[b]]
-        _check_row(o[b], lse[b], np64(q[b]), sel, CK[b], CV[b], np64(k_tok[b]), np64(v_tok[b]),
-                   c - 1, n_win, 1 / math.sqrt(D), f"seq {b} (ctx {c})")
+        _check_row(o[b], lse[b], np64(q[b]), idx[b], CK[b], CV[b], np64(k_tok[b]), np64(v_tok[b]),
+                   c - 1, n_win, m, 1 / math.sqrt(D), f"seq {b} (ctx {c})")
 
 
 def test_tc_decode_hca_two_head_groups_ring_cache():
@@ -103,9 +103,8 @@ def test_tc_decode_hca_two_head_groups_ring_cache():
     o, lse = _decode(p, q, ck, cv, n_cap, None, k_ring, v_ring, ring, ctx_t)
     CK, CV = np64(ck), np64(cv)
     for b, c in enumerate(ctx):
-        ne = O.n_eligible(c - 1, n_win, m)
-        _check_row(o[b], lse[b], np64(q[b]), list(range(ne)), CK[b], CV[b], np64(k_flat[b]),
-                   np64(v_flat[b]), c - 1, n_win, 1 / math.sqrt(D), f"seq {b} (ctx {c})")
+        _check_row(o[b], lse[b], np64(q[b]), None, CK[b], CV[b], np64(k_flat[b]),
+                   np64(v_flat[b]), c - 1, n_win, m, 1 / math.sqrt(D), f"seq {b} (ctx {c})")
 
 
 @pytest.mark.parametrize("kind", ["csa", "hca"])
@@ -142,11 +141,8 @@ def test_tc_prefill_rows_with_own_sets_and_windows(kind):
         K, V = np64(k_tok[b]), np64(v_tok[b])
         for i in range(Tq):
             t = int(pos[b, i])
-            if kind == "csa":
-                sel = [int(j) for j in idx[b, i].cpu() if j >= 0]
-            else:
-                sel = list(range(int(ne[b, i])))
-            _check_row(o[b, i], lse[b, i], np64(q[b, i]), sel, CK[b], CV[b], K, V, t, n_win,
+            _check_row(o[b, i], lse[b, i], np64(q[b, i]), idx[b, i] if kind == "csa" else None,
+                       CK[b], CV[b], K, V, t, n_win, m,
                        1 / math.sqrt(D), f"[{b},{i}] t={t}")
 
 
@@ -165,9 +161,8 @@ def test_tc_decode_overlap_rule_and_explicit_scale():
                      torch.tensor(ctx, dtype=torch.int32, device=DEV))
     CK, CV = np64(ck), np64(cv)
     for b, c in enumerate(ctx):
-        sel = [int(j) for j in idx[b].cpu() if 0 <= j < ne[b]]
-        _check_row(o[b], lse[b], np64(q[b]), sel, CK[b], CV[b], np64(k_tok[b]), np64(v_tok[b]),
-                   c - 1, n_win, scale, f"seq {b}")
+        _check_row(o[b], lse[b], np64(q[b]), idx[b], CK[b], CV[b], np64(k_tok[b]), np64(v_tok[b]),
+                   c - 1, n_win, m, scale, f"seq {b}", rule="overlap")
 
 
 def test_tc_decode_bitwise_repeatable_and_position_invariant():
@@ -226,7 +221,7 @@ def test_tc_decode_hca_long_rows_in_several_cluster_groups(ctx_off):
         vals = np.concatenate([CV[b, :ne], np64(v_ring[b])[win % ring]])
         ro, rl = O.attend(np64(q[b]), keys, vals, 1 / math.sqrt(D))
         assert_close(np64(o[b]), ro, "bf16", f"o[{b}]")
-        assert_close(np64(lse[b]), rl, "bf16", f"lse[{b}]")
+        assert_lse_close(np64(lse[b]), rl, "bf16", f"lse[{b}]")
 
 
 @pytest.mark.parametrize("Bn,k", [(48, 512), (32, 512), (20, 512), (32, 200)])
@@ -245,6 +240,5 @@ def test_tc_decode_split_tails_of_every_size(Bn, k):
     o, lse = _decode(p, q, ck, cv, n_cap, idx.to(DEV), k_tok, v_tok, L, ctx_t)
     CK, CV = np64(ck), np64(cv)
     for b in range(Bn):
-        sel = [int(j) for j in idx[b]]
-        _check_row(o[b], lse[b], np64(q[b]), sel, CK[b], CV[b], np64(k_tok[b]), np64(v_tok[b]),
-                   L - 1, n_win, 1 / math.sqrt(D), f"seq {b}")
+        _check_row(o[b], lse[b], np64(q[b]), idx[b], CK[b], CV[b], np64(k_tok[b]), np64(v_tok[b]),
+                   L - 1, n_win, m, 1 / math.sqrt(D), f"seq {b}")

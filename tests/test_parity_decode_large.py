@@ -23,7 +23,8 @@ import oracle as O
 from long_context_hybrid_02_b300 import binding as B
 from long_context_hybrid_02_b300 import synth
 from long_context_hybrid_02_b300.pipeline import HybridLayer
-from tests._harness import assert_close, assert_sorted_unique, assert_topk_match, np64
+from tests._harness import (assert_close, assert_lse_close, assert_sorted_unique,
+                            assert_topk_match, np64)
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
@@ -108,19 +109,28 @@ def test_csa_attention_stage(csa):
                          tok["k_tok"], tok["v_tok"], layer.tok_cap, qry["ctx_len"], o, lse,
                          (layer.ws.data_ptr(), layer.ws.numel()))
     torch.cuda.synchronize()
-    win = O.window_positions(t, w.n_win)
+    lo = t - w.n_win + 1
     for b in SAMPLE_SEQS:
-        sel = idx[b].cpu().numpy()
-        keys = np.concatenate([np64(ck[b])[sel], np64(tok["k_tok"][b, win[0]:t + 1])])
-        vals = np.concatenate([np64(cv[b])[sel], np64(tok["v_tok"][b, win[0]:t + 1])])
-        ro, rl = O.attend(np64(qry["q"][b, 0]), keys, vals, 1 / math.sqrt(w.d))
+        ro, rl = O.prefill_query(np64(qry["q"][b, 0]), idx[b].cpu().numpy(), np64(ck[b]),
+                                 np64(cv[b]), np64(tok["k_tok"][b, lo:t + 1]),
+                                 np64(tok["v_tok"][b, lo:t + 1]), t, n_win=w.n_win, m=w.m,
+                                 scale=1 / math.sqrt(w.d), tok_base=lo)
         assert_close(np64(o[b]), ro, "bf16", f"o[{b}]")
-        assert_close(np64(lse[b]), rl, "bf16", f"lse[{b}]")
+        assert_lse_close(np64(lse[b]), rl, "bf16", f"lse[{b}]")
 
 
 def test_csa_decode_step_end_to_end(csa):
     """The benchmark's launch sequence; the oracle builds its own caches for two
-    sequences and runs compress -> index -> top-k -> attend in float64."""
+    sequences and runs compress -> index -> top-k -> attend in float64.
+
+    The two sides' compressed indexer keys may differ by one bfloat16 unit in a few
+    elements (float32 against float64 accumulation before the same rounding), which
+    may reorder entries whose scores are within about 1e-6 of each other.  So the
+    step's selection is held to the band rule against oracle scores of the keys the
+    step itself scored (the GPU's compressed indexer keys, already checked against
+    the oracle's at the bfloat16 tolerance), and its attention against the oracle's
+    attention over that selection with the oracle's own caches; the oracle's whole
+    pipeline on its own caches must then give the same o."""
     w, tok, qry, layer = csa
     new_blk = torch.full((w.B,), w.n_blocks - 1, dtype=torch.int32, device=DEV)
     layer.decode_step(qry["q"][:, 0].contiguous(), qry["ctx_len"], new_blk, qry["qI"],
@@ -136,13 +146,21 @@ def test_csa_decode_step_end_to_end(csa):
         o, lse, idx, scores = O.csa_decode(np64(qry["q"][b, 0]), np64(qry["qI"][b, 0]),
                                            np64(qry["w_idx"][b, 0]), ck, cv, cki, K, V, t,
                                            n_win=w.n_win, m=w.m, k=w.k, scale=1 / math.sqrt(w.d))
+        ne = O.n_eligible(t, w.n_win, w.m)
+        gpu_cki = np64(layer.cki[b, :ne])
+        assert_close(gpu_cki, cki[:ne], "bf16", f"cki[{b}]")
+        ref_scores = O.index_scores(np64(qry["qI"][b, 0]), np64(qry["w_idx"][b, 0]), gpu_cki)
+        np.testing.assert_allclose(np64(layer.scores[b, 0, :ne]), ref_scores, rtol=1e-5,
+                                   atol=1e-6 * np.abs(ref_scores).max())
         gi = layer.idx[b, 0].cpu().numpy()
-        overlap = len(set(gi.tolist()) & set(idx.tolist())) / w.k
-        # the two sides' compressed indexer keys may differ by one bfloat16 unit in
-        # a few elements, which can swap entries right at the k-th score
-        assert overlap >= 0.99, overlap
-        assert_close(np64(layer.o[b, 0]), o, "bf16", f"o[{b}]")
-        assert_close(np64(layer.lse[b, 0]), lse, "bf16", f"lse[{b}]")
+        assert_sorted_unique(gi, ne, w.k, f"idx[{b}]")
+        assert_topk_match(gi, O.topk_select(ref_scores, w.k), ref_scores, w.k, f"top-k[{b}]")
+        ro, rl = O.prefill_query(np64(qry["q"][b, 0]), gi, ck, cv, K, V, t, n_win=w.n_win, m=w.m,
+                                 scale=1 / math.sqrt(w.d))
+        assert_close(np64(layer.o[b, 0]), ro, "bf16", f"o[{b}]")
+        assert_lse_close(np64(layer.lse[b, 0]), rl, "bf16", f"lse[{b}]")
+        # the oracle's own selection on its own keys: the same output
+        assert_close(np64(layer.o[b, 0]), o, "bf16", f"o[{b}] (oracle selection)")
 
 
 @pytest.fixture(scope="module")
@@ -184,4 +202,4 @@ def test_hca_decode_step_end_to_end(hca):
         o, lse = O.hca_decode(np64(qry["q"][b, 0]), ck, cv, K, V, t, n_win=w.n_win, m=w.m,
                               scale=1 / math.sqrt(w.d))
         assert_close(np64(layer.o[b, 0]), o, "bf16", f"o[{b}]")
-        assert_close(np64(layer.lse[b, 0]), lse, "bf16", f"lse[{b}]")
+        assert_lse_close(np64(layer.lse[b, 0]), lse, "bf16", f"lse[{b}]")

@@ -21,7 +21,8 @@ import torch
 import oracle as O
 from long_context_hybrid_02_b300 import synth
 from long_context_hybrid_02_b300.pipeline import HybridLayer
-from tests._harness import assert_close, assert_sorted_unique, assert_topk_match, np64
+from tests._harness import (assert_close, assert_lse_close, assert_sorted_unique,
+                            assert_topk_match, np64)
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
@@ -36,15 +37,23 @@ def _check_blocks(w, tok, layer, b, blocks, names):
             assert_close(np64(getattr(layer, cname)[b, j]), ref, "bf16", f"{cname}[{b},{j}]")
 
 
-def _check_attention(q, sel, ck, cv, k_tok, v_tok, t, n_win, o, lse, what):
-    """o/lse of one query against the oracle over compressed rows `sel` + the window."""
-    win = O.window_positions(t, n_win)
-    sel_t = torch.as_tensor(np.asarray(sel, dtype=np.int64), device=ck.device)
-    keys = np.concatenate([np64(ck.index_select(0, sel_t)), np64(k_tok[win[0]:t + 1])])
-    vals = np.concatenate([np64(cv.index_select(0, sel_t)), np64(v_tok[win[0]:t + 1])])
-    ro, rl = O.attend(np64(q), keys, vals, 1 / math.sqrt(q.shape[-1]))
+def _f32(t):
+    """A bfloat16 device tensor as a float32 host array (exact)."""
+    return t.float().cpu().numpy()
+
+
+def _check_attention(w, q, idx, ck, cv, k_tok, v_tok, t, o, lse, what):
+    """o/lse of one query against the oracle: the query's raw index set as the
+    call consumed it (None: HCA, every eligible entry) + its window; the oracle
+    ignores padding and ineligible entries itself.  Only the window's per-token
+    rows are copied to the host."""
+    lo = max(0, t - w.n_win + 1)
+    idx = None if idx is None else idx.cpu().numpy()
+    ro, rl = O.prefill_query(np64(q), idx, _f32(ck), _f32(cv), _f32(k_tok[lo:t + 1]),
+                             _f32(v_tok[lo:t + 1]), t, n_win=w.n_win, m=w.m,
+                             scale=1 / math.sqrt(q.shape[-1]), tok_base=lo)
     assert_close(np64(o), ro, "bf16", what + " o")
-    assert_close(np64(lse), rl, "bf16", what + " lse")
+    assert_lse_close(np64(lse), rl, "bf16", what + " lse")
 
 
 # ------------------------------------------------------------------ CSA prefill chunk
@@ -90,9 +99,9 @@ def test_prefill_attention_sampled_queries(prefill):
     w, tok, qry, layer = prefill
     for i in SAMPLE_Q:
         t = int(qry["q_pos"][0, i])
-        sel = [int(j) for j in layer.idx[0, i].cpu() if j >= 0]
-        _check_attention(qry["q"][0, i], sel, layer.ck[0], layer.cv[0], tok["k_tok"][0],
-                         tok["v_tok"][0], t, w.n_win, layer.o[0, i], layer.lse[0, i], f"[{i}]")
+        _check_attention(w, qry["q"][0, i], layer.idx[0, i], layer.ck[0], layer.cv[0],
+                         tok["k_tok"][0], tok["v_tok"][0], t, layer.o[0, i], layer.lse[0, i],
+                         f"[{i}]")
 
 
 # ------------------------------------------------------------------ CSA decode, 1M tokens
@@ -146,9 +155,9 @@ def test_1m_csa_attention(csa_1m):
     w, tok, qry, layer, planted = csa_1m
     t = w.L - 1
     for b in range(w.B):
-        sel = [int(j) for j in layer.idx[b, 0].cpu() if j >= 0]
-        _check_attention(qry["q"][b, 0], sel, layer.ck[b], layer.cv[b], tok["k_tok"][b],
-                         tok["v_tok"][b], t, w.n_win, layer.o[b, 0], layer.lse[b, 0], f"[{b}]")
+        _check_attention(w, qry["q"][b, 0], layer.idx[b, 0], layer.ck[b], layer.cv[b],
+                         tok["k_tok"][b], tok["v_tok"][b], t, layer.o[b, 0], layer.lse[b, 0],
+                         f"[{b}]")
 
 
 # ------------------------------------------------------------------ HCA decode, 1M tokens
@@ -173,8 +182,6 @@ def test_1m_hca_compress_and_attention(hca_1m):
     _check_blocks(w, tok, layer, 1, list(rng.integers(0, w.n_blocks, 6)) + [w.n_blocks - 1],
                   (("k_tok", "ck"), ("v_tok", "cv")))
     t = w.L - 1
-    ne = O.n_eligible(t, w.n_win, w.m)
     for b in range(w.B):
-        _check_attention(qry["q"][b, 0], list(range(ne)), layer.ck[b], layer.cv[b],
-                         tok["k_tok"][b], tok["v_tok"][b], t, w.n_win, layer.o[b, 0],
-                         layer.lse[b, 0], f"[{b}]")
+        _check_attention(w, qry["q"][b, 0], None, layer.ck[b], layer.cv[b], tok["k_tok"][b],
+                         tok["v_tok"][b], t, layer.o[b, 0], layer.lse[b, 0], f"[{b}]")
