@@ -167,14 +167,10 @@ ha_status csa_topk(const ha_params* p, const float* scores, int32_t n_cap,
  *                <= 0 gives o = 0, lse = -inf for that sequence
  *   o          : T [B, H, d]           lse : float [B, H] or NULL
  *   ws         : ha_workspace_size(p, HA_OP_DECODE, 1, n_cap) bytes (split
- *                partials: the key list is split across CTAs and merged in a
- *                fixed order).  For bfloat16, d = 512 and H a multiple of 64
- *                the splits of a sequence merge inside the kernel, and the size
- *                is 0 (ws may be NULL) unless the sequences are too few to fill
- *                the GPU with one cluster each and their key lists are long
- *                (e.g. 4 sequences of 8,320 keys): then every sequence's keys
- *                are cut into a few cluster ranges whose float32 results go
- *                through ws.
+ *                partials: when the sequences are too few to fill the GPU, each
+ *                key list is cut into splits whose float32 results (o and lse)
+ *                go through ws and are merged in split order by a second
+ *                launch; 0 bytes, ws may be NULL, when there is one split).
  * ------------------------------------------------------------------------- */
 ha_status hybrid_attn_decode(const ha_params* p, const void* q, const void* ck, const void* cv,
                              int32_t n_cap, const int32_t* idx, const void* k_tok,

@@ -35,21 +35,17 @@
 //              the softmax works on S(t), then P(t).V(t);
 //   warps 5-8  softmax of each tile (TMEM lane = key), O^T rescaling, and at the
 //              end of the item the epilogue (TMEM lane = head dim).
-// Rows with one split: persistent grid (one CTA per SM) looping over items.  Rows
-// with 2..8 splits: one item per CTA and the splits of a row form a thread-block
-// cluster; every CTA stages its normalised o in its own shared memory and merges
-// the head dims it owns by reading every split's o from its peers' shared memory
-// (no workspace, no second launch).  Few long rows are cut into G consecutive key
-// ranges of one cluster each, whose float32 results attn_merge combines.
+// Persistent grid (at most one CTA per SM) looping over items.  Rows with one
+// split write o directly.  When the rows are too few to fill the GPU, each row's
+// key list is cut into S splits (one item per CTA); every split writes its
+// normalised o and its lse (float32) to the workspace straight from tensor
+// memory, and attn_merge, chained by programmatic dependent launch, combines the
+// splits of a row in split order.
 // Every wait is bounded (tc::kWaitLimitNs); on timeout the kernel records an error
 // code in the library's device error word and returns.
-#include <cooperative_groups.h>
-
 #include "common.cuh"
 #include "kernels.h"
 #include "tc.cuh"
-
-namespace cg = cooperative_groups;
 
 namespace ha {
 namespace {
@@ -69,8 +65,7 @@ constexpr int kTmemCols = 512;
 constexpr int kSCol = 0;                         // two S buffers: columns [0, 128)
 constexpr int kOCol = 2 * kHG;                   // O^T: 4 x 64 columns [128, 384)
 constexpr int kTokFlag = 1 << 30;                // slot code: per-token row
-constexpr int kMaxClusterSplits = 16;            // splits the in-kernel merge supports
-constexpr int kPreferredClusterSplits = 8;       // splits the launch plan uses at most
+constexpr int kMinSplitKeys = 32;                // fewest keys per split the plan makes
 constexpr float kRescaleLog2 = 8.f;              // P <= 2^8 before the reference moves
 
 constexpr size_t kSmemRing = size_t(kRing) * kStageBytes;
@@ -78,10 +73,6 @@ constexpr size_t kSmemTbl = size_t(4) * 2 * kTile * 4;           // [warp][tile 
 constexpr size_t kSmemMisc = (4 * 64 + 64 + 64 + 2 * 64) * 4 + 32 * 8 + 16;
 constexpr size_t kSmem = 1024 + kQBytes + kSmemRing + kPBytes + kSmemTbl + kSmemMisc;
 static_assert(kSmem <= 232448, "shared-memory budget");
-// the in-cluster merge stages o as bfloat16 [64][512] over the ring and keeps its
-// weights [S][64] and 1/sum [64] in q's space
-static_assert(size_t(kHG) * kD * 2 <= kSmemRing, "merge staging");
-static_assert((kMaxClusterSplits + 1) * kHG * 4 <= kQBytes, "merge weights");
 
 struct TcArgs {
   const bf16* q;         // [rows, H, 512]
@@ -93,19 +84,17 @@ struct TcArgs {
   const int32_t* pos;    // decode: ctx_len [B]; prefill: q_pos [rows]
   int decode, Tq, H, n_cap, tok_cap, n_win, m, k, elig;
   float c;               // softmax scale * log2(e)
-  int S, kps, HG;
-  int G;                 // cluster groups per (row, head group): consecutive key ranges
-  int cluster_merge;     // 1: one item per CTA, splits of a row merged in the cluster
-  long long n_items;     // rows * HG * G * S
-  bf16* o;               // [rows, H, 512]
-  float* lse;            // [rows, H] or null
-  float* o_part;         // G > 1: float32 [rows, G, H, 512], merged by a second launch
-  float* lse_part;       // G > 1: [rows, G, H]
+  int S, kps, HG;       // splits per (row, head group), keys per split, head groups
+  long long n_items;     // rows * HG * S
+  bf16* o;               // [rows, H, 512]        (S == 1)
+  float* lse;            // [rows, H] or null     (S == 1)
+  float* o_part;         // S > 1: float32 [rows, S, H, 512], merged by attn_merge
+  float* lse_part;       // S > 1: [rows, S, H]
   int* err;
 };
 
 struct Item {
-  int r, b, hg, g, split;
+  int r, b, hg, split;
   int t;          // query position
   int ne;         // eligible compressed entries
   int n_c, n_w;   // compressed / window slots of the row's key list
@@ -117,13 +106,11 @@ struct Item {
 __device__ __forceinline__ Item item_head(const TcArgs& a, long long it) {
   Item x;
   x.split = int(it % a.S);
-  long long rest = it / a.S;
-  x.g = int(rest % a.G);
-  rest /= a.G;
+  const long long rest = it / a.S;
   x.hg = int(rest % a.HG);
   x.r = int(rest / a.HG);
   x.b = x.r / a.Tq;
-  x.lo = (x.g * a.S + x.split) * a.kps;
+  x.lo = x.split * a.kps;
   return x;
 }
 
@@ -226,11 +213,6 @@ __device__ __forceinline__ float warp_transpose_reduce32(const float (&v)[32], O
 
 struct MaxOp { __device__ float operator()(float x, float y) const { return fmaxf(x, y); } };
 
-// Four bfloat16 (two 32-bit words, low half first) as floats.
-__device__ __forceinline__ float4 bf16x4_to_f4(uint2 u) {
-  return make_float4(__uint_as_float(u.x << 16), __uint_as_float(u.x & 0xffff0000u),
-                     __uint_as_float(u.y << 16), __uint_as_float(u.y & 0xffff0000u));
-}
 struct AddOp { __device__ float operator()(float x, float y) const { return x + y; } };
 
 __global__ void __launch_bounds__(kThreads, 1) attn_decode_tc(const TcArgs a) {
@@ -584,7 +566,30 @@ __global__ void __launch_bounds__(kThreads, 1) attn_decode_tc(const TcArgs a) {
         }
       }
       tc::named_barrier(1, 128);
-      if (a.cluster_merge) break;             // the only item: O^T leaves after the cluster barrier
+      if (a.S > 1) {
+        // one split of the row: o = O^T / l and lse as float32 partials, merged by
+        // attn_merge (lane = head dim: a warp stores 128 contiguous bytes per head)
+        const long long prow = ((long long)x.r * a.S + x.split) * a.H + x.hg * kHG;
+#pragma unroll 1
+        for (int half = 0; half < 2; ++half) {
+          float sc[32];
+#pragma unroll
+          for (int h = 0; h < 32; ++h) sc[h] = stats[half * 32 + h];
+#pragma unroll 1
+          for (int mb = 0; mb < kD / 128; ++mb) {
+            float v[32];
+            tc::tmem_ld32(tmem + t_lane + kOCol + mb * kHG + half * 32, v);
+            float* dst = a.o_part + (prow + half * 32) * kD + mb * 128 + row;
+#pragma unroll
+            for (int h = 0; h < 32; ++h) dst[(long long)h * kD] = v[h] * sc[h];
+          }
+        }
+        if (sw < 2) a.lse_part[prow + sw * 32 + lane] = stats[64 + sw * 32 + lane];
+        tc::fence_before_sync();
+        tc::mbar_arrive(o_empty);
+        tc::named_barrier(1, 128);
+        continue;
+      }
       const long long hrow = (long long)x.r * a.H + x.hg * kHG;   // first head of the group
       // 1/l of the 32 heads of a half in registers before any store (the stores
       // could otherwise alias them and serialise every load)
@@ -608,132 +613,6 @@ __global__ void __launch_bounds__(kThreads, 1) attn_decode_tc(const TcArgs a) {
       tc::mbar_arrive(o_empty);
       tc::named_barrier(1, 128);              // stats and mref are rewritten by the next item
     }
-  }
-  tc::fence_before_sync();
-  __syncthreads();
-  if (a.cluster_merge) {
-    // Every CTA of the cluster holds one split of the same query row and head group.
-    // Each CTA stages its normalised o as bfloat16 [64 heads][512 dims] over its idle
-    // ring, with the eight warps that can read its tensor memory (warps 0-3 and 5-8;
-    // lanes = consecutive dims).  After a cluster barrier, CTA r merges the dims
-    // [lo(r), lo(r + 1)), lo(r) = 4 floor(128 r / S), reading every split's o and
-    // lse from the peers' shared memory (8-byte loads, 256 contiguous bytes per
-    // warp), in split order and in float32:
-    //   o = sum_s exp(lse_s - mx) o_s / sum_s exp(lse_s - mx),  lse = mx + log(sum).
-    // The exchange between SMs is the slow part of the merge (its bandwidth is far
-    // below the SM's own shared memory), so o_s crosses it in bfloat16: o is a convex
-    // combination of the o_s, so the rounding adds at most 2^-9 max_s |o_s|.
-    // A last barrier keeps every CTA's shared memory alive until its peers are done.
-    tc::fence_after_sync();
-    cg::cluster_group cluster = cg::this_cluster();
-    const Item x = item_of(a, blockIdx.x);
-    const int S = a.S, me = x.split;
-    bf16* stage_o = reinterpret_cast<bf16*>(ring);            // [64][512] (the idle ring)
-    float* wts = reinterpret_cast<float*>(sQ);                // [S][64] (q is idle now)
-    float* inv = wts + kMaxClusterSplits * kHG;               // [64]
-    if (warp != 4) {
-      const int quarter = warp & 3, half = warp < 4 ? 1 : 0;
-      const uint32_t t_lane = uint32_t(quarter * 32) << 16;
-      float sc[32];
-#pragma unroll
-      for (int h = 0; h < 32; ++h) sc[h] = stats[half * 32 + h];
-      bf16* dst = stage_o + half * 32 * kD + quarter * 32 + lane;
-#pragma unroll 1
-      for (int mb = 0; mb < kD / 128; mb += 2) {
-        float va[32], vb[32];
-        tc::tmem_ld32x2(tmem + t_lane + kOCol + mb * kHG + half * 32,
-                        tmem + t_lane + kOCol + (mb + 1) * kHG + half * 32, va, vb);
-#pragma unroll
-        for (int h = 0; h < 32; ++h) {
-          dst[h * kD + mb * 128] = __float2bfloat16_rn(va[h] * sc[h]);
-          dst[h * kD + mb * 128 + 128] = __float2bfloat16_rn(vb[h] * sc[h]);
-        }
-      }
-    }
-    cluster.sync();                                           // every split is staged
-    const int h0 = x.hg * kHG;
-    const uint32_t stats_lse = tc::smem_u32(stats + 64);
-    if (threadIdx.x < kHG) {
-      const int h = threadIdx.x;
-      float l[kMaxClusterSplits];
-#pragma unroll
-      for (int s2 = 0; s2 < kMaxClusterSplits; ++s2)
-        l[s2] = s2 < S ? tc::ld_cluster_f32(tc::mapa_shared(stats_lse + 4 * h, s2)) : -INFINITY;
-      float mx = -INFINITY;
-#pragma unroll
-      for (int s2 = 0; s2 < kMaxClusterSplits; ++s2) mx = fmaxf(mx, l[s2]);
-      float tot = 0.f;
-#pragma unroll
-      for (int s2 = 0; s2 < kMaxClusterSplits; ++s2) {
-        if (s2 < S) {
-          const float wv = mx == -INFINITY ? 0.f : expf(l[s2] - mx);
-          wts[s2 * kHG + h] = wv;
-          tot += wv;
-        }
-      }
-      inv[h] = tot > 0.f ? 1.f / tot : 0.f;
-      const float lse_m = tot > 0.f ? mx + logf(tot) : -INFINITY;
-      if (me == 0) {
-        if (a.G > 1) a.lse_part[((long long)x.r * a.G + x.g) * a.H + h0 + h] = lse_m;
-        else if (a.lse) a.lse[(long long)x.r * a.H + h0 + h] = lse_m;
-      }
-    }
-    __syncthreads();
-    const int g_lo = me * (kD / 4) / S, g_hi = (me + 1) * (kD / 4) / S;
-    const int width = g_hi - g_lo;                            // 4-dim groups of this CTA
-    const int n_out = kHG * width;
-    const uint32_t stage_base = tc::smem_u32(stage_o);
-    // two outputs per thread and pass; every split's loads of both are issued
-    // before the first is used (four splits at a time)
-    for (int i = threadIdx.x; i < n_out; i += 2 * kThreads) {
-      const int i2 = min(i + kThreads, n_out - 1);
-      const int hA = i / width, gA = i % width, hB = i2 / width, gB = i2 % width;
-      const uint32_t offA = stage_base + 2u * uint32_t(hA * kD + 4 * (g_lo + gA));
-      const uint32_t offB = stage_base + 2u * uint32_t(hB * kD + 4 * (g_lo + gB));
-      float4 accA = make_float4(0.f, 0.f, 0.f, 0.f), accB = accA;
-      for (int s0 = 0; s0 < S; s0 += 4) {
-        float4 va[4], vb[4];
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          if (s0 + u < S) {
-            va[u] = bf16x4_to_f4(tc::ld_cluster_u2(tc::mapa_shared(offA, s0 + u)));
-            vb[u] = bf16x4_to_f4(tc::ld_cluster_u2(tc::mapa_shared(offB, s0 + u)));
-          }
-        }
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          if (s0 + u < S) {
-            const float wa = wts[(s0 + u) * kHG + hA], wb = wts[(s0 + u) * kHG + hB];
-            accA.x = fmaf(wa, va[u].x, accA.x);
-            accA.y = fmaf(wa, va[u].y, accA.y);
-            accA.z = fmaf(wa, va[u].z, accA.z);
-            accA.w = fmaf(wa, va[u].w, accA.w);
-            accB.x = fmaf(wb, vb[u].x, accB.x);
-            accB.y = fmaf(wb, vb[u].y, accB.y);
-            accB.z = fmaf(wb, vb[u].z, accB.z);
-            accB.w = fmaf(wb, vb[u].w, accB.w);
-          }
-        }
-      }
-      auto put = [&](int h, int g4, const float4& acc) {
-        const float iv = inv[h];
-        if (a.G > 1) {                                        // partial of this group
-          *reinterpret_cast<float4*>(a.o_part + (((long long)x.r * a.G + x.g) * a.H + h0 + h) * kD +
-                                     4 * (g_lo + g4)) =
-              make_float4(acc.x * iv, acc.y * iv, acc.z * iv, acc.w * iv);
-          return;
-        }
-        const __nv_bfloat162 lo2 = __floats2bfloat162_rn(acc.x * iv, acc.y * iv);
-        const __nv_bfloat162 hi2 = __floats2bfloat162_rn(acc.z * iv, acc.w * iv);
-        uint2 pk;
-        pk.x = *reinterpret_cast<const uint32_t*>(&lo2);
-        pk.y = *reinterpret_cast<const uint32_t*>(&hi2);
-        *reinterpret_cast<uint2*>(a.o + ((long long)x.r * a.H + h0 + h) * kD + 4 * (g_lo + g4)) = pk;
-      };
-      put(hA, gA, accA);
-      if (i + kThreads < n_out) put(hB, gB, accB);
-    }
-    cluster.sync();                                           // peers are done reading
   }
   tc::fence_before_sync();
   __syncthreads();
@@ -761,109 +640,25 @@ bool attention_tc_supported(const ha_params& p, int n_cap, int tok_cap) {
          (long long)p.B * n_cap < kTokFlag && (long long)p.B * tok_cap < kTokFlag;
 }
 
-// Largest cluster (number of splits merged in the kernel) the current device can
-// schedule with this kernel's resources: 16 needs the non-portable cluster size.
-int max_cluster_splits() {
-  static int cached[64] = {};
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 8;
-  if (cached[dev] != 0) return cached[dev];
-  int best = 8;
-  if (ensure_smem(reinterpret_cast<const void*>(attn_decode_tc), kSmem) == cudaSuccess &&
-      cudaFuncSetAttribute(reinterpret_cast<const void*>(attn_decode_tc),
-                           cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess) {
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(kMaxClusterSplits);
-    cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = kSmem;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = kMaxClusterSplits;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, attn_decode_tc, &cfg) == cudaSuccess && n > 0)
-      best = kMaxClusterSplits;
-  }
-  (void)cudaGetLastError();
-  cached[dev] = best;
-  return best;
-}
-
-// Clusters of S CTAs of this kernel that the device keeps resident at once (0 when
-// the query fails).  Clusters need their SMs inside one GPC, so large clusters
-// pack worse than small ones.
-int active_clusters(int S) {
-  static int cached[64][kMaxClusterSplits + 1] = {};
-  int dev = 0;
-  if (S < 1 || S > kMaxClusterSplits) return 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
-  if (cached[dev][S] != 0) return cached[dev][S] > 0 ? cached[dev][S] : 0;
-  int n = 0;
-  if (ensure_smem(reinterpret_cast<const void*>(attn_decode_tc), kSmem) == cudaSuccess &&
-      (S <= 8 || cudaFuncSetAttribute(reinterpret_cast<const void*>(attn_decode_tc),
-                                      cudaFuncAttributeNonPortableClusterSizeAllowed,
-                                      1) == cudaSuccess)) {
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(unsigned(S));
-    cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = kSmem;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = unsigned(S);
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    if (cudaOccupancyMaxActiveClusters(&n, attn_decode_tc, &cfg) != cudaSuccess) n = 0;
-  }
-  (void)cudaGetLastError();
-  cached[dev][S] = n > 0 ? n : -1;
-  return n > 0 ? n : 0;
-}
-
 AttnPlan plan_attention_tc(const ha_params& p, int rows, int max_keys) {
   AttnPlan pl{};
   const long long units = (long long)rows * (p.H / kHG);
   const int sms = num_sms();
-  // enough splits to cover the SMs, at most what one cluster merges
-  // (8 = the portable cluster size: clusters of 16 need a whole GPC each and fewer of
-  // them are resident at a time, which measured slower on B300)
+  // Enough splits per (row, head group) that the items cover the SMs in one wave,
+  // but at least kMinSplitKeys keys per split (every split also loads q, 64 KiB).
   int S = units >= sms ? 1 : int(sms / units);
-  if (S > kPreferredClusterSplits) S = kPreferredClusterSplits;
-  if (S > max_cluster_splits()) S = max_cluster_splits();
+  const int by_keys = max_keys / kMinSplitKeys;
+  if (S > by_keys) S = by_keys;
   if (S < 1) S = 1;
-  // all clusters resident at once (a second wave would double the time)
-  while (S > 1 && active_clusters(S) > 0 && units > active_clusters(S)) --S;
-  // When the clusters still leave half the GPU idle and every split would walk
-  // more than two tiles (few long rows: HCA at 1M tokens), each row's keys are
-  // cut into G consecutive ranges of one cluster each, clusters of 4 (they pack
-  // into the GPCs better than clusters of 8, of which fewer are resident); the G
-  // cluster results (float32, with their lse) are merged by a second launch.
-  int G = 1;
-  if (S > 1 && units * S * 2 <= sms && (max_keys + S - 1) / S > 2 * kTile) {
-    S = S < 4 ? S : 4;
-    G = int(sms / (units * S));
-    const int fit = active_clusters(S);
-    if (fit > 0 && G > fit / units) G = int(fit / units);
-    const int g_keys = (max_keys + S * 2 * kTile - 1) / (S * 2 * kTile);
-    if (G > g_keys) G = g_keys;
-    if (G < 1) G = 1;
-  }
-  int kps = (max_keys + S * G - 1) / (S * G);
+  int kps = (max_keys + S - 1) / S;
   kps = (kps + 15) / 16 * 16;
   if (kps < 16) kps = 16;
-  if (G == 1) {
-    S = (max_keys + kps - 1) / kps;
-    if (S < 1) S = 1;
-  }
+  S = (max_keys + kps - 1) / kps;
+  if (S < 1) S = 1;
   pl.n_splits = S;
   pl.keys_per_split = kps;
   pl.tile = kTile;
-  pl.n_groups = G;
-  pl.ws_bytes = G > 1 ? size_t(rows) * G * p.H * (kD + 1) * sizeof(float) : 0;
+  pl.ws_bytes = S > 1 ? size_t(rows) * S * p.H * (kD + 1) * sizeof(float) : 0;
   return pl;
 }
 
@@ -895,25 +690,21 @@ cudaError_t launch_attention_tc(const ha_params& p, const AttnPlan& pl, int deco
   a.kps = pl.keys_per_split;
   a.HG = p.H / kHG;
   const int rows = p.B * Tq;
-  a.G = pl.n_groups > 1 && a.S > 1 ? pl.n_groups : 1;
-  a.n_items = (long long)rows * a.S * a.G * a.HG;
+  a.n_items = (long long)rows * a.S * a.HG;
   a.o = static_cast<bf16*>(o);
   a.lse = lse;
   a.err = err;
-  a.cluster_merge = a.S > 1 ? 1 : 0;
-  if (a.G > 1) {
+  if (a.S > 1) {
     if (ws == nullptr) return cudaErrorInvalidValue;
     a.o_part = static_cast<float*>(ws);
-    a.lse_part = a.o_part + (long long)rows * a.G * p.H * kD;
+    a.lse_part = a.o_part + (long long)rows * a.S * p.H * kD;
   }
   cudaError_t e = ensure_smem(reinterpret_cast<const void*>(attn_decode_tc), kSmem);
   if (e != cudaSuccess) return e;
-  const long long grid = a.cluster_merge ? a.n_items                    // one item per CTA
-                                         : (a.n_items < num_sms() ? a.n_items : num_sms());
-  e = launch_pdl(attn_decode_tc, dim3(unsigned(grid)), dim3(kThreads), kSmem, st,
-                 a.cluster_merge ? unsigned(a.S) : 1u, a);
-  if (e != cudaSuccess || a.G == 1) return e;
-  return launch_attn_merge(p, rows, a.G, a.o_part, a.lse_part, o, lse, st);
+  const long long grid = a.n_items < num_sms() ? a.n_items : num_sms();
+  e = launch_pdl(attn_decode_tc, dim3(unsigned(grid)), dim3(kThreads), kSmem, st, 1u, a);
+  if (e != cudaSuccess || a.S == 1) return e;
+  return launch_attn_merge(p, rows, a.S, a.o_part, a.lse_part, o, lse, st);
 }
 
 }  // namespace ha

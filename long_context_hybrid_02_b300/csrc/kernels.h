@@ -46,11 +46,10 @@ cudaError_t launch_topk(const ha_params& p, const float* scores, int n_cap, cons
 
 // attention.cu: split-KV CUDA-core attention (decode and prefill) + merge.
 struct AttnPlan {
-  int n_splits;        // key-list ranges per query row (per cluster group, tensor cores)
+  int n_splits;        // key-list ranges per query row (and 64-head group, tensor cores)
   int keys_per_split;  // multiple of 32 (CUDA cores) / 16 (tensor cores)
   int tile;            // keys staged per shared-memory tile
-  size_t ws_bytes;     // float32 partials when n_splits > 1 (CUDA cores) or n_groups > 1
-  int n_groups;        // tensor cores: cluster groups per row and head group (0 or 1: one)
+  size_t ws_bytes;     // float32 partials when n_splits > 1
 };
 AttnPlan plan_attention_simt(const ha_params& p, int rows, int max_keys, bool decode);
 cudaError_t launch_attention_simt(const ha_params& p, const AttnPlan& pl, int decode, int Tq,

@@ -111,20 +111,25 @@ def test_attention_validation(lib):
                    None, 0) == 2
 
 
-def test_attention_workspace_only_for_cluster_groups(lib):
-    """The tensor-core decode attention merges a row's splits inside one cluster
-    (no workspace) unless few long rows are cut into several cluster groups,
-    whose float32 results (o and lse per head) go through the workspace.  On a
-    machine without a GPU the plan assumes 148 SMs, as on the B300."""
-    def ws(Bn, H, n_cap, csa):
-        p = B.make_params(Bn, H, 512, 128, 4 if csa else 128, 1024 if csa else 1,
+def test_attention_workspace_holds_the_split_partials(lib):
+    """The tensor-core decode attention cuts every row's key list into S splits
+    when the rows are too few to fill the GPU (S = floor(148 / (rows x H/64)), at
+    least 32 keys per split, keys per split rounded up to 16); each split's float32
+    o and lse per head go through the workspace: rows x S x H x (512 + 1) floats.
+    On a machine without a GPU the plan assumes 148 SMs, as on the B300."""
+    def ws(Bn, H, n_cap, csa, k=1024):
+        p = B.make_params(Bn, H, 512, 128, 4 if csa else 128, k if csa else 1,
                           64 if csa else 1, 128 if csa else 8, B.BF16)
         return B.ha_workspace_size(p, B.OP_DECODE, 1, n_cap, csa)
-    assert ws(32, 64, 16384, True) == 0          # 64K CSA: 32 rows x 4 splits
-    assert ws(32, 64, 1024, False) == 0          # 128K HCA
-    assert ws(4, 128, 262144, True) == 0         # 1M CSA: 1,152 keys, 8 splits
-    # 1M HCA: 8 units x 4 groups of 4-CTA clusters; rows x G x H x (512 + 1) floats
-    assert ws(4, 128, 8192, False) == 4 * 4 * 128 * 513 * 4
+    # 64K CSA (k = 512): 32 rows x 4 splits of 160 keys (512 + 128)
+    assert ws(32, 64, 16384, True, k=512) == 32 * 4 * 64 * 513 * 4
+    assert ws(160, 64, 1024, False) == 0         # 160 rows >= 148 SMs: one split each
+    # 128K HCA: 32 rows x 4 splits of 288 keys (1,024 + 128 -> 1,152)
+    assert ws(32, 64, 1024, False) == 32 * 4 * 64 * 513 * 4
+    # 1M CSA: 4 rows x 2 head groups; 18 splits of 64 keys (1,024 + 128)
+    assert ws(4, 128, 262144, True) == 4 * 18 * 128 * 513 * 4
+    # 1M HCA: 18 splits of 464 keys (8,192 + 128)
+    assert ws(4, 128, 8192, False) == 4 * 18 * 128 * 513 * 4
 
 
 def test_workspace_sizes(lib):

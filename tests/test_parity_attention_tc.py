@@ -187,9 +187,8 @@ def test_tc_decode_bitwise_repeatable_and_position_invariant():
 @pytest.mark.parametrize("ctx_off", [(0, 77), (0, 77, L_LONG - 200, L_LONG)])
 def test_tc_decode_hca_long_rows_in_several_cluster_groups(ctx_off):
     """Up to 6,144 + 128 keys per row and few rows: every row's keys are cut into
-    several consecutive ranges of one 8-CTA cluster each, whose float32 results
-    are merged by a second launch; a 200-token and an empty context leave whole
-    ranges without keys."""
+    many splits whose float32 results are merged by a second launch; a 200-token
+    and an empty context leave whole splits without keys."""
     m, n_win, ring = 128, 128, 256
     n_cap = 6144
     L = n_cap * m

@@ -75,12 +75,14 @@ def _run_both(w, p, tok, q, ck, cv, idx, n_cap, ctx_len):
 
 @pytest.mark.gpu
 @pytest.mark.parametrize("kind,dtype,B_,L,H,d,k,uses_scratch", [
-    # tensor cores, 8 rows: the splits of a row merge inside one cluster (no scratch)
-    ("csa", "bf16", 8, 16384, 64, 512, 512, False),
-    ("hca", "bf16", 4, 65536, 64, 512, 1, False),        # 511 + 128 keys per row
-    # tensor cores, one row of 2,047 + 128 keys: the row is cut into several
-    # cluster groups whose float32 results go through the scratch
+    # tensor cores: few rows, so every row's keys are cut into splits whose float32
+    # partials go through the scratch (8 rows of 512 + 128 keys, 4 rows of 511 + 128,
+    # one row of 2,047 + 128)
+    ("csa", "bf16", 8, 16384, 64, 512, 512, True),
+    ("hca", "bf16", 4, 65536, 64, 512, 1, True),
     ("hca", "bf16", 1, 262144, 64, 512, 1, True),
+    # tensor cores, 160 rows: one split per row, written directly (no scratch)
+    ("hca", "bf16", 160, 4096, 64, 512, 1, False),
     # CUDA cores: split partials of every row go through the scratch
     ("csa", "f32", 2, 1024, 8, 64, 16, True),
 ])
