@@ -4,10 +4,11 @@
 Default workload: CSA decode, 32 sequences at 65,536 tokens, 64 query heads of
 dim 512 on one shared K/V head, window 128, m = 4 (16,384 entries per
 sequence), top-512, indexer 64 heads x 128, bfloat16 storage, fp32 accumulation.
-One step = one decode token per sequence through the whole path: compress the
-block completed by the newest token (on a side stream: under the disjoint
-eligibility rule that block is not visible to the step's own query), score every
-eligible entry, select the top-k, attend to selection + window.  The step's launches are
+One step = one decode token per sequence through the whole path, as one call of
+the library's fused decode step: compress the block completed by the newest
+token (under the disjoint eligibility rule that block is not visible to the step's
+own query, so scoring runs beside it), score every eligible entry, select the
+top-k, attend to selection + window.  The step's launches are
 captured once in a CUDA graph and replayed; timing uses CUDA events recorded at
 both ends of the graph on the launching stream, with an L2 flush (256 MiB write,
 then 256 MiB read) before every timed step.  The library's kernels are chained
@@ -637,13 +638,19 @@ def main():
     concurrent_compress = layer.p.elig == B.ELIG_DISJOINT and w.n_win >= w.m
 
     def step(marks: bool):
-        """One decode step.  The first and last events are always recorded; with
-        marks, also one between every two calls (the per-kernel breakdown: a
-        recorded event between two kernels also keeps the second from starting
-        early, so the headline graph has none), and the calls run one after the
-        other; without, the compression runs on a side stream."""
+        """One decode step.  The first and last events are always recorded.  Without
+        marks (the headline) the step is one fused library call, csa_decode_step /
+        hca_decode_step: compress the block the newest token completes, score,
+        select, attend, chained on the stream.  With marks the same kernels run as
+        the separate calls, one after the other, with an event between every two
+        (the per-kernel breakdown: a recorded event between two kernels also keeps
+        the second from starting early)."""
         s = stream.cuda_stream
         ev[0].record(stream)
+        if not marks:
+            layer.decode_step_fused(q, qry["ctx_len"], qry.get("qI"), qry.get("w_idx"), s)
+            ev[n_ev - 1].record(stream)
+            return
         overlap = concurrent_compress and not marks
         if not overlap:
             layer.compress(new_blk, 1, s)

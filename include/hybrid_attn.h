@@ -77,7 +77,7 @@ typedef enum {
 
 typedef enum { HA_F32 = 0, HA_BF16 = 1 } ha_dtype;
 typedef enum { HA_ELIG_DISJOINT = 0, HA_ELIG_OVERLAP = 1 } ha_elig;
-typedef enum { HA_OP_TOPK = 0, HA_OP_DECODE = 1, HA_OP_PREFILL = 2 } ha_op;
+typedef enum { HA_OP_TOPK = 0, HA_OP_DECODE = 1, HA_OP_PREFILL = 2, HA_OP_DECODE_STEP = 3 } ha_op;
 
 /* Layer description.  Limits: 1 <= B; 1 <= H <= 256; 8 <= d <= 1024, d % 8 == 0;
  * 1 <= n_win <= 65536; 1 <= m <= 1024; 1 <= k <= 4096 (CSA); 1 <= H_I <= 128;
@@ -102,6 +102,7 @@ typedef struct {
  *   k_tok, v_tok : T [B, tok_cap, d]      per-token K and V
  *   gate         : float [B, tok_cap]     one gate logit per token
  *   blk_begin    : int32 [B]              first block to compress per sequence
+ *                                         (negative: none of its blocks)
  *   n_blk        : blocks per sequence (>= 0; 0 is a no-op)
  *   ck, cv       : T [B, n_cap, d]        rows blk_begin[b] .. +n_blk-1 written
  * Block j reads positions j*m .. j*m+m-1 (the caller guarantees they are
@@ -192,6 +193,51 @@ ha_status hybrid_attn_prefill(const ha_params* p, const void* q, const int32_t* 
                               const int32_t* idx, const void* k_tok, const void* v_tok,
                               int32_t tok_cap, void* o, float* lse, void* ws, size_t ws_bytes,
                               ha_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * csa_decode_step -- one decode token per sequence through a whole SWA + CSA
+ * layer in one call, in the pages' order ([V4-notes] §5.3: compress, score every
+ * compressed entry with the Lightning Indexer, select the top k, attend to them
+ * and to the window; §11.4: the tail tokens of an unfinished block stay in the
+ * per-token cache until the block completes):
+ *   1. if the newest token completes a block (ctx_len % m == 0), that block,
+ *      (ctx_len / m) - 1, is compressed into ck, cv, cki;
+ *   2. csa_index_scores, 3. csa_topk and 4. hybrid_attn_decode for the query at
+ *      t = ctx_len - 1.
+ * The results are those of the four calls issued in that order (the same
+ * kernels): scores, idx, o and lse as documented there.  The caller writes the
+ * newest token's rows (k_tok, v_tok, ki_tok, gate at slot (ctx_len-1) % tok_cap)
+ * before the call.  The kernels are chained with programmatic dependent launch;
+ * under the disjoint rule with n_win >= m no stage reads the block the step
+ * compresses, so scoring runs beside the compression and the attention requests
+ * q before the selection is final.
+ *   q      : T [B, H, d]         q_idx : T [B, H_I, d_I]     w_idx : float [B, H_I]
+ *   k_tok, v_tok : T [B, tok_cap, d]    ki_tok : T [B, tok_cap, d_I]
+ *   gate   : float [B, tok_cap]  ctx_len : int32 [B]  (tok_cap >= max(n_win, m))
+ *   ck, cv : T [B, n_cap, d]     cki : T [B, n_cap, d_I]
+ *   scores : float [B, n_cap]    idx : int32 [B, k]
+ *   o      : T [B, H, d]         lse : float [B, H] or NULL
+ *   ws     : ha_workspace_size(p, HA_OP_DECODE_STEP, 1, n_cap, 1) bytes
+ * ------------------------------------------------------------------------- */
+ha_status csa_decode_step(const ha_params* p, const void* q, const void* q_idx,
+                          const float* w_idx, const void* k_tok, const void* v_tok,
+                          const void* ki_tok, const float* gate, int32_t tok_cap,
+                          const int32_t* ctx_len, void* ck, void* cv, void* cki, int32_t n_cap,
+                          float* scores, int32_t* idx, void* o, float* lse, void* ws,
+                          size_t ws_bytes, ha_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * hca_decode_step -- one decode token per sequence through a whole SWA + HCA
+ * layer ([V4-notes] §5.4): the block completed by the newest token (if any) is
+ * compressed into ck, cv, then hybrid_attn_decode attends to every eligible
+ * entry and the window.  Arguments as csa_decode_step; ws is
+ * ha_workspace_size(p, HA_OP_DECODE_STEP, 1, n_cap, 0) bytes.  Under the disjoint
+ * rule with n_win >= m the attention runs beside the compression.
+ * ------------------------------------------------------------------------- */
+ha_status hca_decode_step(const ha_params* p, const void* q, const void* k_tok, const void* v_tok,
+                          const float* gate, int32_t tok_cap, const int32_t* ctx_len, void* ck,
+                          void* cv, int32_t n_cap, void* o, float* lse, void* ws, size_t ws_bytes,
+                          ha_stream_t stream);
 
 /* ---------------------------------------------------------------------------
  * hybrid_attn_decode_static -- hybrid_attn_decode without a workspace argument,

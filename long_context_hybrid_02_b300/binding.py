@@ -16,7 +16,7 @@ LIB_PATH = os.path.join(_PKG, "libhybridattn.so")
 
 F32, BF16 = 0, 1
 ELIG_DISJOINT, ELIG_OVERLAP = 0, 1
-OP_TOPK, OP_DECODE, OP_PREFILL = 0, 1, 2
+OP_TOPK, OP_DECODE, OP_PREFILL, OP_DECODE_STEP = 0, 1, 2, 3
 STATUS = {0: "HA_OK", 1: "HA_ERR_INVALID_ARG", 2: "HA_ERR_MISALIGNED", 3: "HA_ERR_UNSUPPORTED",
           4: "HA_ERR_WORKSPACE", 5: "HA_ERR_CUDA"}
 
@@ -51,6 +51,10 @@ _SIGS = {
                            _P, _SZ, _P],
     "hybrid_attn_prefill": [ctypes.POINTER(Params), _P, _P, _I, _P, _P, _I, _P, _P, _P, _I, _P,
                             _P, _P, _SZ, _P],
+    "csa_decode_step": [ctypes.POINTER(Params), _P, _P, _P, _P, _P, _P, _P, _I, _P, _P, _P, _P, _I,
+                        _P, _P, _P, _P, _P, _SZ, _P],
+    "hca_decode_step": [ctypes.POINTER(Params), _P, _P, _P, _P, _I, _P, _P, _P, _I, _P, _P, _P,
+                        _SZ, _P],
     "hybrid_attn_decode_static": [ctypes.POINTER(Params), _P, _P, _P, _I, _P, _P, _P, _I, _P, _P,
                                   _P, _P],
     "ha_workspace_size": [ctypes.POINTER(Params), _I, _I, _I, _I, ctypes.POINTER(ctypes.c_size_t)],
@@ -153,6 +157,22 @@ def hybrid_attn_prefill(p, q, q_pos, Tq, ck, cv, n_cap, idx, k_tok, v_tok, tok_c
     wp, wb = _ws(ws)
     _call("hybrid_attn_prefill", ctypes.byref(p), _ptr(q), _ptr(q_pos), Tq, _ptr(ck), _ptr(cv),
           n_cap, _ptr(idx), _ptr(k_tok), _ptr(v_tok), tok_cap, _ptr(o), _ptr(lse), wp, wb,
+          _stream(stream))
+
+
+def csa_decode_step(p, q, q_idx, w_idx, k_tok, v_tok, ki_tok, gate, tok_cap, ctx_len, ck, cv,
+                    cki, n_cap, scores, idx, o, lse=None, ws=None, stream=None):
+    wp, wb = _ws(ws)
+    _call("csa_decode_step", ctypes.byref(p), _ptr(q), _ptr(q_idx), _ptr(w_idx), _ptr(k_tok),
+          _ptr(v_tok), _ptr(ki_tok), _ptr(gate), tok_cap, _ptr(ctx_len), _ptr(ck), _ptr(cv),
+          _ptr(cki), n_cap, _ptr(scores), _ptr(idx), _ptr(o), _ptr(lse), wp, wb, _stream(stream))
+
+
+def hca_decode_step(p, q, k_tok, v_tok, gate, tok_cap, ctx_len, ck, cv, n_cap, o, lse=None,
+                    ws=None, stream=None):
+    wp, wb = _ws(ws)
+    _call("hca_decode_step", ctypes.byref(p), _ptr(q), _ptr(k_tok), _ptr(v_tok), _ptr(gate),
+          tok_cap, _ptr(ctx_len), _ptr(ck), _ptr(cv), n_cap, _ptr(o), _ptr(lse), wp, wb,
           _stream(stream))
 
 

@@ -184,6 +184,38 @@ ha_status compress_common(const ha_params* p, int n_tensors, const void* const* 
 
 }  // namespace
 
+namespace {
+
+size_t round_up256(size_t x) { return (x + 255) / 256 * 256; }
+
+// Workspace of a fused decode step: the top-k part (segmented rows), then the
+// attention partials.
+size_t step_workspace_bytes(const ha_params* p, int n_cap, int tok_cap, bool is_csa) {
+  const size_t topk = is_csa ? round_up256(ha::topk_workspace_bytes(*p, 1, n_cap)) : 0;
+  return topk + attention_plan(p, p->B, n_cap, tok_cap, is_csa, true).ws_bytes;
+}
+
+// Checks shared by the two fused decode steps (everything but the indexer inputs).
+ha_status check_step(const ha_params* p, const void* q, const void* k_tok, const void* v_tok,
+                     const float* gate, int32_t tok_cap, const int32_t* ctx_len, const void* ck,
+                     const void* cv, int32_t n_cap, const void* o, const float* lse) {
+  HA_PTR(q);
+  HA_PTR(k_tok);
+  HA_PTR(v_tok);
+  HA_PTR4(gate);
+  HA_PTR4(ctx_len);
+  HA_PTR(ck);
+  HA_PTR(cv);
+  HA_PTR(o);
+  HA_OPT_PTR4(lse);
+  HA_REQUIRE(n_cap >= 1, HA_ERR_INVALID_ARG, "n_cap = %d", n_cap);
+  HA_REQUIRE(tok_cap >= p->n_win && tok_cap >= p->m, HA_ERR_INVALID_ARG,
+             "tok_cap = %d < max(n_win = %d, m = %d)", tok_cap, p->n_win, p->m);
+  return HA_OK;
+}
+
+}  // namespace
+
 size_t ha::decode_workspace_bytes(const ha_params* p, int n_cap, int tok_cap, bool is_csa) {
   return attention_plan(p, p->B, n_cap, tok_cap, is_csa, true).ws_bytes;
 }
@@ -194,7 +226,7 @@ void ha::set_last_error(const char* msg) {
 
 extern "C" {
 
-int32_t ha_abi_version(void) { return 1; }
+int32_t ha_abi_version(void) { return 2; }
 
 uint64_t ha_launch_count(void) { return ha::launch_count(); }
 
@@ -380,6 +412,116 @@ ha_status hybrid_attn_prefill(const ha_params* p, const void* q, const int32_t* 
                      "prefill launch");
 }
 
+ha_status csa_decode_step(const ha_params* p, const void* q, const void* q_idx,
+                          const float* w_idx, const void* k_tok, const void* v_tok,
+                          const void* ki_tok, const float* gate, int32_t tok_cap,
+                          const int32_t* ctx_len, void* ck, void* cv, void* cki, int32_t n_cap,
+                          float* scores, int32_t* idx, void* o, float* lse, void* ws,
+                          size_t ws_bytes, ha_stream_t stream) {
+  g_last_error[0] = 0;
+  CallRange range("csa_decode_step");
+  ha_status s = check_params(p, true, true);
+  if (s != HA_OK) return s;
+  s = check_k(p);
+  if (s != HA_OK) return s;
+  s = check_step(p, q, k_tok, v_tok, gate, tok_cap, ctx_len, ck, cv, n_cap, o, lse);
+  if (s != HA_OK) return s;
+  HA_PTR(q_idx);
+  HA_PTR4(w_idx);
+  HA_PTR(ki_tok);
+  HA_PTR(cki);
+  HA_PTR4(scores);
+  HA_PTR4(idx);
+  HA_OPT_PTR(ws);
+  HA_REQUIRE(n_cap <= ha::topk_max_row_entries(), HA_ERR_UNSUPPORTED, "n_cap = %d > %d", n_cap,
+             ha::topk_max_row_entries());
+  const size_t topk_ws = round_up256(ha::topk_workspace_bytes(*p, 1, n_cap));
+  const ha::AttnPlan pl = attention_plan(p, p->B, n_cap, tok_cap, true, true);
+  const size_t need = topk_ws + pl.ws_bytes;
+  HA_REQUIRE(ws_bytes >= need && (need == 0 || ws != nullptr), HA_ERR_WORKSPACE,
+             "workspace %zu bytes < %zu", ws_bytes, need);
+  int* err = ha::device_error_word();
+  HA_REQUIRE(err != nullptr, HA_ERR_CUDA, "device error word unavailable");
+  const cudaStream_t st = (cudaStream_t)stream;
+  // Under the disjoint rule with n_win >= m the block the newest token completes
+  // ends inside the query's window, so no stage of this step reads it: scoring
+  // starts while it is compressed (the indexer waits for the compressor only
+  // before it exits).  Otherwise the stages run strictly in order.
+  const bool overlap = p->elig == HA_ELIG_DISJOINT && p->n_win >= p->m;
+  ha::StepOpts sc;
+  sc.ctx_len = ctx_len;
+  const void* src[3] = {k_tok, v_tok, ki_tok};
+  void* dst[3] = {ck, cv, cki};
+  const int dims[3] = {p->d, p->d, p->d_I};
+  cudaError_t e = ha::launch_compress(*p, 3, src, dst, dims, gate, nullptr, 1, tok_cap, n_cap, st, sc);
+  if (e != cudaSuccess) return cuda_status(e, "step: compress launch");
+  ha::StepOpts si;
+  si.pos_off = -1;
+  if (ha::index_scores_tc_supported(*p, q_idx, cki)) {
+    si.wait_last = overlap ? 1 : 0;
+    e = ha::launch_index_scores_tc(*p, q_idx, w_idx, cki, n_cap, ctx_len, 1, scores, err, st, si);
+  } else {
+    e = ha::launch_index_scores_simt(*p, q_idx, w_idx, cki, n_cap, ctx_len, 1, scores, st, si);
+  }
+  if (e != cudaSuccess) return cuda_status(e, "step: index launch");
+  ha::StepOpts sk;
+  sk.pos_off = -1;
+  e = ha::launch_topk(*p, scores, n_cap, ctx_len, 1, idx, ws, topk_ws, st, sk);
+  if (e != cudaSuccess) return cuda_status(e, "step: top-k launch");
+  void* attn_ws = pl.ws_bytes ? static_cast<char*>(ws) + topk_ws : nullptr;
+  if (ha::attention_tc_supported(*p, n_cap, tok_cap)) {
+    ha::StepOpts sa;
+    sa.early = 1;
+    e = ha::launch_attention_tc(*p, pl, 1, 1, q, ctx_len, ck, cv, n_cap, idx, k_tok, v_tok,
+                                tok_cap, o, lse, attn_ws, err, st, sa);
+  } else {
+    e = ha::launch_attention_simt(*p, pl, 1, 1, q, ctx_len, ck, cv, n_cap, idx, k_tok, v_tok,
+                                  tok_cap, o, lse, attn_ws, st);
+  }
+  return cuda_status(e, "step: attention launch");
+}
+
+ha_status hca_decode_step(const ha_params* p, const void* q, const void* k_tok, const void* v_tok,
+                          const float* gate, int32_t tok_cap, const int32_t* ctx_len, void* ck,
+                          void* cv, int32_t n_cap, void* o, float* lse, void* ws, size_t ws_bytes,
+                          ha_stream_t stream) {
+  g_last_error[0] = 0;
+  CallRange range("hca_decode_step");
+  ha_status s = check_params(p, true, false);
+  if (s != HA_OK) return s;
+  s = check_step(p, q, k_tok, v_tok, gate, tok_cap, ctx_len, ck, cv, n_cap, o, lse);
+  if (s != HA_OK) return s;
+  HA_OPT_PTR(ws);
+  const ha::AttnPlan pl = attention_plan(p, p->B, n_cap, tok_cap, false, true);
+  HA_REQUIRE(ws_bytes >= pl.ws_bytes && (pl.ws_bytes == 0 || ws != nullptr), HA_ERR_WORKSPACE,
+             "workspace %zu bytes < %zu", ws_bytes, pl.ws_bytes);
+  const cudaStream_t st = (cudaStream_t)stream;
+  // As in csa_decode_step: under the disjoint rule with n_win >= m the attention
+  // reads no entry the compressor writes, so it runs beside the compression and
+  // waits for it only before it exits.  (Launching the attention first and the
+  // compressor beside it on the SMs it leaves was measured slower.)
+  const bool overlap = p->elig == HA_ELIG_DISJOINT && p->n_win >= p->m;
+  ha::StepOpts sc;
+  sc.ctx_len = ctx_len;
+  const void* src[2] = {k_tok, v_tok};
+  void* dst[2] = {ck, cv};
+  const int dims[2] = {p->d, p->d};
+  cudaError_t e = ha::launch_compress(*p, 2, src, dst, dims, gate, nullptr, 1, tok_cap, n_cap, st, sc);
+  if (e != cudaSuccess) return cuda_status(e, "step: compress launch");
+  if (ha::attention_tc_supported(*p, n_cap, tok_cap)) {
+    int* err = ha::device_error_word();
+    HA_REQUIRE(err != nullptr, HA_ERR_CUDA, "device error word unavailable");
+    ha::StepOpts sa;
+    sa.wait_last = overlap ? 1 : 0;
+    e = ha::launch_attention_tc(*p, pl, 1, 1, q, ctx_len, ck, cv, n_cap, nullptr, k_tok, v_tok,
+                                tok_cap, o, lse, ws, err, st, sa);
+  } else {
+    e = ha::launch_attention_simt(*p, pl, 1, 1, q, ctx_len, ck, cv, n_cap, nullptr, k_tok, v_tok,
+                                  tok_cap, o, lse, ws, st);
+  }
+  return cuda_status(e, "step: attention launch");
+}
+
 ha_status ha_workspace_size(const ha_params* p, int32_t op, int32_t Tq, int32_t n_cap,
                             int32_t is_csa, size_t* bytes) {
   g_last_error[0] = 0;
@@ -395,6 +537,9 @@ ha_status ha_workspace_size(const ha_params* p, int32_t op, int32_t Tq, int32_t 
       return HA_OK;
     case HA_OP_PREFILL:
       *bytes = attention_plan(p, p->B * Tq, n_cap, 0, is_csa != 0, false).ws_bytes;
+      return HA_OK;
+    case HA_OP_DECODE_STEP:
+      *bytes = step_workspace_bytes(p, n_cap, 0, is_csa != 0);
       return HA_OK;
   }
   return fail(HA_ERR_INVALID_ARG, "op = %d", op);

@@ -91,6 +91,8 @@ struct TcArgs {
   float* o_part;         // S > 1: float32 [rows, S, H, 512], merged by attn_merge
   float* lse_part;       // S > 1: [rows, S, H]
   int* err;
+  int early;             // fused step: q and positions are read before the wait, idx after it
+  int wait_last;         // fused step: nothing read comes from the previous kernel
 };
 
 struct Item {
@@ -255,7 +257,16 @@ __global__ void __launch_bounds__(kThreads, 1) attn_decode_tc(const TcArgs a) {
   __syncthreads();
   tc::fence_after_sync();
   const uint32_t tmem = *tmem_slot;
-  pdl_wait_then_release();                  // the set-up above touched no global memory
+  // The set-up above touched no global memory.  Stand-alone calls wait for the
+  // previous kernel here.  Inside a fused decode step q and the positions are
+  // inputs of the step (final before its first kernel passed its own wait), so in
+  // the CSA step the producer requests q first and waits only before it reads the
+  // selection, the softmax warps before their first selection read; in the HCA
+  // step nothing the kernel reads comes from the previous kernel (the compressor,
+  // which writes a block no query of the step sees), so it waits only before it
+  // exits.
+  if (a.early || a.wait_last) pdl_release();
+  else pdl_wait_then_release();
 
   if (warp < 4) {
     // ------------------------------------------------------------------ producer
@@ -304,6 +315,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_decode_tc(const TcArgs a) {
       }
       tc::cp_async_commit();
       q_pending = true;
+      if (a.early && n == 0) pdl_wait();      // the selection comes from the previous kernel
       int ent0[kTile / 32];
 #pragma unroll
       for (int j = 0; j < kTile / 32; ++j) ent0[j] = slot_entry(a, x, x.lo + lane + 32 * j);
@@ -451,6 +463,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_decode_tc(const TcArgs a) {
     const int rsw = row & 7;
     long long n = 0, G = 0;
     bool ok = true;
+    if (a.early) pdl_wait();                  // slot_entry reads the selection
     for (long long it = blockIdx.x; it < a.n_items && ok; it += gridDim.x, ++n) {
       const Item x = item_of(a, it);
       // this warp's share of the per-head sums of P: heads lane and 32 + lane
@@ -617,6 +630,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_decode_tc(const TcArgs a) {
   tc::fence_before_sync();
   __syncthreads();
   if (warp == 4) tc::tmem_dealloc(tmem, kTmemCols);
+  if (a.wait_last) pdl_wait();
 }
 
 int g_num_sms[64] = {};
@@ -666,8 +680,10 @@ cudaError_t launch_attention_tc(const ha_params& p, const AttnPlan& pl, int deco
                                 const void* q, const int32_t* pos, const void* ck, const void* cv,
                                 int n_cap, const int32_t* idx, const void* k_tok,
                                 const void* v_tok, int tok_cap, void* o, float* lse, void* ws,
-                                int* err, cudaStream_t st) {
+                                int* err, cudaStream_t st, const StepOpts& so) {
   TcArgs a{};
+  a.early = so.early;
+  a.wait_last = so.wait_last;
   a.q = static_cast<const bf16*>(q);
   a.ck = static_cast<const bf16*>(ck);
   a.cv = static_cast<const bf16*>(cv);

@@ -55,6 +55,14 @@ __device__ __forceinline__ void pdl_wait_then_release() {
   asm volatile("griddepcontrol.wait;" ::: "memory");
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
+// The two halves, for kernels of a fused step that read nothing the previous
+// kernel writes: they let the next kernel be scheduled at once and wait for the
+// previous one only before they exit, so that their completion still implies the
+// completion of everything before them in the stream.
+__device__ __forceinline__ void pdl_release() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
 // ---------------------------------------------------------------- storage types
 template <typename T> struct Elem;

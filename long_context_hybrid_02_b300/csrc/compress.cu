@@ -25,8 +25,18 @@ struct CompressArgs {
   int n_tensors;
   const float* gate;
   const int32_t* blk_begin;
+  const int32_t* ctx_len;   // non-null: the block the newest token completes (n_blk = 1)
   int B, n_blk, m, tok_cap, n_cap;
 };
+
+// First block to compress for sequence b: blk_begin[b], or the block completed by
+// the newest token (ctx_len[b] / m - 1 when ctx_len[b] is a positive multiple of m,
+// else none).  Negative: none of the sequence's blocks is compressed.
+__device__ __forceinline__ int first_block(const CompressArgs& a, int b) {
+  if (!a.ctx_len) return a.blk_begin[b];
+  const int c = a.ctx_len[b];
+  return (c > 0 && c % a.m == 0) ? c / a.m - 1 : -1;
+}
 
 template <typename T>
 __device__ __forceinline__ void locate(const CompressArgs& a, int c, int& tsr, int& chunk) {
@@ -47,7 +57,8 @@ __global__ void __launch_bounds__(256) compress_small_m(CompressArgs a) {
     const int c = int(it % total_chunks);
     const long long task = it / total_chunks;
     const int b = int(task / a.n_blk);
-    const int j = a.blk_begin[b] + int(task % a.n_blk);
+    const int fb = first_block(a, b);
+    const int j = fb < 0 ? -1 : fb + int(task % a.n_blk);
     if (j < 0 || j >= a.n_cap) continue;
     int tsr, chunk;
     locate<T>(a, c, tsr, chunk);
@@ -113,7 +124,8 @@ __global__ void __launch_bounds__(512) compress_large_m(CompressArgs a) {
   float* part = sm + ((a.m + 3) & ~3);
   const int task = blockIdx.x;
   const int b = task / a.n_blk;
-  const int j = a.blk_begin[b] + task % a.n_blk;
+  const int fb = first_block(a, b);
+  const int j = fb < 0 ? -1 : fb + task % a.n_blk;
   if (j < 0 || j >= a.n_cap) return;                // uniform over the CTA
   const int lane_c = threadIdx.x % kSlice;          // chunk within the slice
   const int grp = threadIdx.x / kSlice;             // token group
@@ -211,8 +223,9 @@ cudaError_t launch(const CompressArgs& a, cudaStream_t st) {
 cudaError_t launch_compress(const ha_params& p, int n_tensors, const void* const* src,
                             void* const* dst, const int* dims, const float* gate,
                             const int32_t* blk_begin, int n_blk, int tok_cap, int n_cap,
-                            cudaStream_t st) {
+                            cudaStream_t st, const StepOpts& so) {
   CompressArgs a{};
+  a.ctx_len = so.ctx_len;
   const int V = p.dtype == HA_BF16 ? 8 : 4;
   for (int i = 0; i < 3; ++i) {
     a.src[i] = i < n_tensors ? src[i] : nullptr;

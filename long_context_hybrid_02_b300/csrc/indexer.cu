@@ -17,6 +17,7 @@ __global__ void __launch_bounds__(256) index_scores_simt(const T* __restrict__ q
                                                          const float* __restrict__ w,
                                                          const T* __restrict__ cI, int n_cap,
                                                          const int32_t* __restrict__ q_pos,
+                                                         int pos_off,
                                                          int Tq, int H_I, int d_I, int n_win,
                                                          int m, int elig,
                                                          float* __restrict__ scores) {
@@ -26,7 +27,7 @@ __global__ void __launch_bounds__(256) index_scores_simt(const T* __restrict__ q
   float* sw = sq + H_I * d_I;
   const int row = blockIdx.x;                      // b * Tq + t
   const int b = row / Tq;
-  const int t = q_pos[row];
+  const int t = q_pos[row] + pos_off;
   const int ne = n_eligible(t, n_win, m, elig, n_cap);
   const int j0 = blockIdx.y * blockDim.x;
   if (j0 >= ne) return;                            // uniform
@@ -56,7 +57,7 @@ __global__ void __launch_bounds__(256) index_scores_simt(const T* __restrict__ q
 
 cudaError_t launch_index_scores_simt(const ha_params& p, const void* q_idx, const float* w_idx,
                                      const void* cki, int n_cap, const int32_t* q_pos, int Tq,
-                                     float* scores, cudaStream_t st) {
+                                     float* scores, cudaStream_t st, const StepOpts& so) {
   const dim3 grid(p.B * Tq, (n_cap + 255) / 256);
   const size_t smem = (size_t(p.H_I) * p.d_I + p.H_I) * sizeof(float);
   if (p.dtype == HA_BF16) {
@@ -64,14 +65,15 @@ cudaError_t launch_index_scores_simt(const ha_params& p, const void* q_idx, cons
     cudaError_t e = ensure_smem(reinterpret_cast<const void*>(k), smem);
     if (e != cudaSuccess) return e;
     return launch_pdl(k, grid, dim3(256), smem, st, 1, static_cast<const __nv_bfloat16*>(q_idx),
-                      w_idx, static_cast<const __nv_bfloat16*>(cki), n_cap, q_pos, Tq, p.H_I,
+                      w_idx, static_cast<const __nv_bfloat16*>(cki), n_cap, q_pos, so.pos_off, Tq, p.H_I,
                       p.d_I, p.n_win, p.m, p.elig, scores);
   } else {
     auto k = index_scores_simt<float>;
     cudaError_t e = ensure_smem(reinterpret_cast<const void*>(k), smem);
     if (e != cudaSuccess) return e;
     return launch_pdl(k, grid, dim3(256), smem, st, 1, static_cast<const float*>(q_idx), w_idx,
-                      static_cast<const float*>(cki), n_cap, q_pos, Tq, p.H_I, p.d_I, p.n_win,
+                      static_cast<const float*>(cki), n_cap, q_pos, so.pos_off, Tq, p.H_I, p.d_I,
+                      p.n_win,
                       p.m, p.elig, scores);
   }
 }

@@ -51,10 +51,12 @@ static_assert(Cfg<1>::kSmem <= 232448 && Cfg<4>::kSmem <= 232448, "shared-memory
 
 struct IdxArgs {
   const float* w;          // [B*Tq, H_I]
-  const int32_t* q_pos;    // [B*Tq]
+  const int32_t* q_pos;    // [B*Tq]; query position = q_pos + pos_off
   float* scores;           // [B*Tq, n_cap]
   int B, Tq, n_cap, n_win, m, elig;
   int* err;
+  int pos_off;
+  int wait_last;           // fused step: wait for the previous kernel only before exiting
 };
 
 // Tiles of group g = (b, qg): ceil(max n_elig over its queries / 128).
@@ -65,7 +67,8 @@ __device__ __forceinline__ int group_tiles(const IdxArgs& a, int g) {
   int ne = 0;
 #pragma unroll
   for (int q = 0; q < QT; ++q)
-    if (q0 + q < a.Tq) ne = max(ne, n_eligible(a.q_pos[b * a.Tq + q0 + q], a.n_win, a.m, a.elig, a.n_cap));
+    if (q0 + q < a.Tq)
+      ne = max(ne, n_eligible(a.q_pos[b * a.Tq + q0 + q] + a.pos_off, a.n_win, a.m, a.elig, a.n_cap));
   return (ne + kTileM - 1) / kTileM;
 }
 
@@ -135,7 +138,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     index_scores_tc(const __grid_constant__ CUtensorMap map_k,
                     const __grid_constant__ CUtensorMap map_q, IdxArgs a) {
   using C = Cfg<QT>;
-  pdl_wait_then_release();
+  if (a.wait_last) pdl_release();
+  else pdl_wait_then_release();
   extern __shared__ unsigned char smem_raw[];
   unsigned char* base = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -253,7 +257,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
 #pragma unroll
         for (int q = 0; q < QT; ++q)
-          ne_q[q] = q0 + q < a.Tq ? n_eligible(a.q_pos[b * a.Tq + q0 + q], a.n_win, a.m, a.elig, a.n_cap) : 0;
+          ne_q[q] = q0 + q < a.Tq
+                        ? n_eligible(a.q_pos[b * a.Tq + q0 + q] + a.pos_off, a.n_win, a.m, a.elig, a.n_cap)
+                        : 0;
         if constexpr (QT == 1) {
 #pragma unroll
           for (int h = 0; h < kHeads; ++h) w_reg[h] = w_mine[h];
@@ -299,6 +305,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc::fence_before_sync();
   __syncthreads();
   if (warp == 1) tc::tmem_dealloc(tmem, C::kTmemCols);
+  if (a.wait_last) pdl_wait();
 }
 
 int g_num_sms = 0;
@@ -306,7 +313,7 @@ int g_num_sms = 0;
 template <int QT>
 cudaError_t launch_qt(const ha_params& p, const void* q_idx, const float* w_idx, const void* cki,
                       int n_cap, const int32_t* q_pos, int Tq, float* scores, int* err,
-                      cudaStream_t st) {
+                      cudaStream_t st, const StepOpts& so) {
   using C = Cfg<QT>;
   CUtensorMap map_k, map_q;
   cudaError_t e = make_tmap_bf16_2d(&map_k, cki, kDim, uint64_t(p.B) * n_cap, kDim * 2, 64, kTileM);
@@ -321,7 +328,8 @@ cudaError_t launch_qt(const ha_params& p, const void* q_idx, const float* w_idx,
     e = cudaDeviceGetAttribute(&g_num_sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return e;
   }
-  IdxArgs a{w_idx, q_pos, scores, p.B, Tq, n_cap, p.n_win, p.m, p.elig, err};
+  IdxArgs a{w_idx, q_pos, scores, p.B, Tq, n_cap, p.n_win, p.m, p.elig, err, so.pos_off,
+            so.wait_last};
   return launch_pdl(index_scores_tc<QT>, dim3(g_num_sms), dim3(kThreads), C::kSmem, st, 1, map_k,
                     map_q, a);
 }
@@ -335,9 +343,9 @@ bool index_scores_tc_supported(const ha_params& p, const void* q_idx, const void
 
 cudaError_t launch_index_scores_tc(const ha_params& p, const void* q_idx, const float* w_idx,
                                    const void* cki, int n_cap, const int32_t* q_pos, int Tq,
-                                   float* scores, int* err, cudaStream_t st) {
-  if (Tq >= 4) return launch_qt<4>(p, q_idx, w_idx, cki, n_cap, q_pos, Tq, scores, err, st);
-  return launch_qt<1>(p, q_idx, w_idx, cki, n_cap, q_pos, Tq, scores, err, st);
+                                   float* scores, int* err, cudaStream_t st, const StepOpts& so) {
+  if (Tq >= 4) return launch_qt<4>(p, q_idx, w_idx, cki, n_cap, q_pos, Tq, scores, err, st, so);
+  return launch_qt<1>(p, q_idx, w_idx, cki, n_cap, q_pos, Tq, scores, err, st, so);
 }
 
 }  // namespace ha

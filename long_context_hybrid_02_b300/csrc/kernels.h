@@ -9,6 +9,18 @@
 
 namespace ha {
 
+// How a kernel of a fused decode step (csa_decode_step / hca_decode_step) is tied
+// to the previous kernel of the stream; the defaults are the stand-alone calls.
+struct StepOpts {
+  int pos_off = 0;                   // query position = pos + pos_off (-1: pos is ctx_len)
+  int wait_last = 0;                 // reads nothing the previous kernel writes: release
+                                     // the next kernel at once, wait only before exiting
+  int early = 0;                     // attention: q and the positions are read before the
+                                     // wait (they are inputs of the step, final by then)
+  const int32_t* ctx_len = nullptr;  // compressor: compress the block the newest token
+                                     // completes (block ctx_len/m - 1 when ctx_len % m == 0)
+};
+
 // api.cu: replace the message returned by ha_last_error() on this thread.
 void set_last_error(const char* msg);
 
@@ -25,24 +37,27 @@ int* device_error_word();
 cudaError_t launch_compress(const ha_params& p, int n_tensors, const void* const* src,
                             void* const* dst, const int* dims, const float* gate,
                             const int32_t* blk_begin, int n_blk, int tok_cap, int n_cap,
-                            cudaStream_t st);
+                            cudaStream_t st, const StepOpts& so = StepOpts());
 
 // indexer.cu: CUDA-core indexer for every shape and type.
 cudaError_t launch_index_scores_simt(const ha_params& p, const void* q_idx, const float* w_idx,
                                      const void* cki, int n_cap, const int32_t* q_pos, int Tq,
-                                     float* scores, cudaStream_t st);
+                                     float* scores, cudaStream_t st,
+                                     const StepOpts& so = StepOpts());
 
 // indexer_tc.cu: tcgen05 indexer for bf16, H_I = 64, d_I = 128.
 bool index_scores_tc_supported(const ha_params& p, const void* q_idx, const void* cki);
 cudaError_t launch_index_scores_tc(const ha_params& p, const void* q_idx, const float* w_idx,
                                    const void* cki, int n_cap, const int32_t* q_pos, int Tq,
-                                   float* scores, int* err, cudaStream_t st);
+                                   float* scores, int* err, cudaStream_t st,
+                                   const StepOpts& so = StepOpts());
 
 // topk.cu
 size_t topk_workspace_bytes(const ha_params& p, int Tq, int n_cap);
 int topk_max_row_entries();       // longest score row csa_topk supports
 cudaError_t launch_topk(const ha_params& p, const float* scores, int n_cap, const int32_t* q_pos,
-                        int Tq, int32_t* idx, void* ws, size_t ws_bytes, cudaStream_t st);
+                        int Tq, int32_t* idx, void* ws, size_t ws_bytes, cudaStream_t st,
+                        const StepOpts& so = StepOpts());
 
 // attention.cu: split-KV CUDA-core attention (decode and prefill) + merge.
 struct AttnPlan {
@@ -69,6 +84,6 @@ cudaError_t launch_attention_tc(const ha_params& p, const AttnPlan& pl, int deco
                                 const void* q, const int32_t* pos, const void* ck, const void* cv,
                                 int n_cap, const int32_t* idx, const void* k_tok,
                                 const void* v_tok, int tok_cap, void* o, float* lse, void* ws,
-                                int* err, cudaStream_t st);
+                                int* err, cudaStream_t st, const StepOpts& so = StepOpts());
 
 }  // namespace ha

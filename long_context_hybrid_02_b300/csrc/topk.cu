@@ -142,14 +142,14 @@ __device__ __forceinline__ void row_radix(RowShared& sh, int count, int k, KeyAt
 
 __global__ void __launch_bounds__(kRowThreads) topk_row(const float* __restrict__ scores,
                                                        int n_cap, const int32_t* __restrict__ q_pos,
-                                                       int k, int n_win, int m, int elig,
-                                                       int32_t* __restrict__ idx) {
+                                                       int pos_off, int k, int n_win, int m,
+                                                       int elig, int32_t* __restrict__ idx) {
   extern __shared__ uint32_t skeys[];
   __shared__ RowShared sh;
   pdl_wait_then_release();
   const int row = blockIdx.x;
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
-  const int n = n_eligible(q_pos[row], n_win, m, elig, n_cap);
+  const int n = n_eligible(q_pos[row] + pos_off, n_win, m, elig, n_cap);
   int32_t* out = idx + (long long)row * k;
   if (n <= k) {                                   // every eligible entry, then -1
     for (int i = tid; i < k; i += kRowThreads) out[i] = i < n ? i : -1;
@@ -304,7 +304,8 @@ struct SegMeta {
 
 __global__ void __launch_bounds__(kRowThreads) topk_seg(const float* __restrict__ scores,
                                                        int n_cap, const int32_t* __restrict__ q_pos,
-                                                       int k, int n_win, int m, int elig, int C,
+                                                       int pos_off, int k, int n_win, int m,
+                                                       int elig, int C,
                                                        int seg_len, SegMeta* __restrict__ meta,
                                                        uint2* __restrict__ cand) {
   extern __shared__ uint32_t skeys[];
@@ -312,7 +313,7 @@ __global__ void __launch_bounds__(kRowThreads) topk_seg(const float* __restrict_
   pdl_wait_then_release();
   const int row = blockIdx.x / C, c = blockIdx.x % C;
   const int tid = threadIdx.x;
-  const int n = n_eligible(q_pos[row], n_win, m, elig, n_cap);
+  const int n = n_eligible(q_pos[row] + pos_off, n_win, m, elig, n_cap);
   const int lo = min(n, c * seg_len), hi = min(n, lo + seg_len), len = hi - lo;
   if (n <= k || len == 0) {                       // nothing to keep
     if (tid == 0) meta[blockIdx.x] = SegMeta{0, 0u};
@@ -372,8 +373,8 @@ __global__ void __launch_bounds__(kRowThreads) topk_seg(const float* __restrict_
 }
 
 __global__ void __launch_bounds__(kRowThreads) topk_seg_merge(
-    const float* __restrict__ scores, int n_cap, const int32_t* __restrict__ q_pos, int k,
-    int n_win, int m, int elig, int C, const SegMeta* __restrict__ meta,
+    const float* __restrict__ scores, int n_cap, const int32_t* __restrict__ q_pos, int pos_off,
+    int k, int n_win, int m, int elig, int C, const SegMeta* __restrict__ meta,
     const uint2* __restrict__ cand, int32_t* __restrict__ idx) {
   extern __shared__ uint32_t smem[];
   __shared__ RowShared sh;
@@ -381,7 +382,7 @@ __global__ void __launch_bounds__(kRowThreads) topk_seg_merge(
   __shared__ uint32_t s_gmax;
   pdl_wait_then_release();
   const int row = blockIdx.x, tid = threadIdx.x;
-  const int n = n_eligible(q_pos[row], n_win, m, elig, n_cap);
+  const int n = n_eligible(q_pos[row] + pos_off, n_win, m, elig, n_cap);
   int32_t* out = idx + (long long)row * k;
   if (n <= k) {
     for (int i = tid; i < k; i += kRowThreads) out[i] = i < n ? i : -1;
@@ -534,7 +535,8 @@ size_t topk_workspace_bytes(const ha_params& p, int Tq, int n_cap) {
 }
 
 cudaError_t launch_topk(const ha_params& p, const float* scores, int n_cap, const int32_t* q_pos,
-                        int Tq, int32_t* idx, void* ws, size_t ws_bytes, cudaStream_t st) {
+                        int Tq, int32_t* idx, void* ws, size_t ws_bytes, cudaStream_t st,
+                        const StepOpts& so) {
   const long long rows = (long long)p.B * Tq;
   if (rows == 0) return cudaSuccess;
   if (n_cap <= kRowMaxKeys) {                     // the row fits one CTA's shared memory
@@ -542,7 +544,7 @@ cudaError_t launch_topk(const ha_params& p, const float* scores, int n_cap, cons
     cudaError_t e = ensure_smem(reinterpret_cast<const void*>(topk_row), smem);
     if (e != cudaSuccess) return e;
     return launch_pdl(topk_row, dim3(unsigned(rows)), dim3(kRowThreads), smem, st, 1u, scores,
-                      n_cap, q_pos, p.k, p.n_win, p.m, p.elig, idx);
+                      n_cap, q_pos, so.pos_off, p.k, p.n_win, p.m, p.elig, idx);
   }
   if (n_cap <= kMaxSegRowKeys) {                  // segments, then one merge per row
     const SegPlan sp = seg_plan(rows, n_cap, num_sms());
@@ -554,13 +556,14 @@ cudaError_t launch_topk(const ha_params& p, const float* scores, int n_cap, cons
     cudaError_t e = ensure_smem(reinterpret_cast<const void*>(topk_seg), smem1);
     if (e != cudaSuccess) return e;
     e = launch_pdl(topk_seg, dim3(unsigned(rows * sp.C)), dim3(kRowThreads), smem1, st, 1u, scores,
-                   n_cap, q_pos, p.k, p.n_win, p.m, p.elig, sp.C, sp.seg_len, meta, cand);
+                   n_cap, q_pos, so.pos_off, p.k, p.n_win, p.m, p.elig, sp.C, sp.seg_len, meta,
+                   cand);
     if (e != cudaSuccess) return e;
     const size_t smem2 = (size_t(2) * kMergeCap + sp.C + 1) * sizeof(uint32_t);
     e = ensure_smem(reinterpret_cast<const void*>(topk_seg_merge), smem2);
     if (e != cudaSuccess) return e;
     return launch_pdl(topk_seg_merge, dim3(unsigned(rows)), dim3(kRowThreads), smem2, st, 1u,
-                      scores, n_cap, q_pos, p.k, p.n_win, p.m, p.elig, sp.C,
+                      scores, n_cap, q_pos, so.pos_off, p.k, p.n_win, p.m, p.elig, sp.C,
                       static_cast<const SegMeta*>(meta), static_cast<const uint2*>(cand), idx);
   }
   return cudaErrorNotSupported;                  // rows longer than kMaxSegRowKeys

@@ -5,14 +5,20 @@ selected indices, outputs, workspace) and issues the library calls of a decode
 step or a prefill chunk in the order the method runs them: compress the block
 that just completed -> score every eligible entry -> select the top k -> attend
 to the selection plus the window (CSA); compress -> attend to every eligible
-entry plus the window (HCA).  Torch only allocates memory and provides the
-stream; every step runs in the library's CUDA kernels.
+entry plus the window (HCA).  `decode_step_fused` issues the same stages through
+one call (csa_decode_step / hca_decode_step).  With a `CacheState` the layer also
+takes ragged appends of new tokens into ring-buffered per-token caches and
+compresses the blocks they complete.  Torch only allocates memory, copies the
+caller's new token rows into their cache slots and provides the stream; every
+stage of the method runs in the library's CUDA kernels.
 """
 from __future__ import annotations
 
+import numpy as np
 import torch
 
 from . import binding as B
+from .cache_state import CacheState
 from .synth import Workload
 
 
@@ -24,7 +30,7 @@ def params_for(w: Workload, Tq_override: int | None = None) -> B.Params:
 
 class HybridLayer:
     def __init__(self, w: Workload, tokens: dict, device="cuda", n_cap: int | None = None,
-                 tok_cap: int | None = None):
+                 tok_cap: int | None = None, state: CacheState | None = None):
         self.w = w
         self.device = device
         self.p = params_for(w)
@@ -45,6 +51,9 @@ class HybridLayer:
         nb = B.ha_workspace_size(self.p, op, Tq, self.n_cap, self.csa)
         if self.csa:
             nb = max(nb, B.ha_workspace_size(self.p, B.OP_TOPK, Tq, self.n_cap, True))
+        if w.decode:
+            nb = max(nb, B.ha_workspace_size(self.p, B.OP_DECODE_STEP, 1, self.n_cap, self.csa))
+        self.state = state
         self.ws = torch.empty((max(nb, 16),), dtype=torch.uint8, device=device)
         self.blk_zero = torch.zeros((w.B,), dtype=torch.int32, device=device)
         # side stream for the decode step's compression (see decode_step)
@@ -105,6 +114,43 @@ class HybridLayer:
         if joined:
             main.wait_event(self._join)
         return self.o
+
+    def decode_step_fused(self, q, ctx_len, qI=None, w_idx=None, stream=None):
+        """The decode step through one library call: the block completed by the
+        newest token (if any) is compressed, then (CSA) scoring, selection and
+        attention.  The newest token's rows must already be in the per-token caches."""
+        t = self.tok
+        ws = (self.ws.data_ptr(), self.ws.numel())
+        if self.csa:
+            B.csa_decode_step(self.p, q, qI, w_idx, t["k_tok"], t["v_tok"], t["ki_tok"], t["gate"],
+                              self.tok_cap, ctx_len, self.ck, self.cv, self.cki, self.n_cap,
+                              self.scores, self.idx, self.o, self.lse, ws, stream)
+        else:
+            B.hca_decode_step(self.p, q, t["k_tok"], t["v_tok"], t["gate"], self.tok_cap, ctx_len,
+                              self.ck, self.cv, self.n_cap, self.o, self.lse, ws, stream)
+        return self.o
+
+    def append(self, rows: dict, n_new, stream=None):
+        """Append n_new[b] tokens to sequence b ([V4-notes] §11.4: the tokens of an
+        unfinished block stay in the per-token cache, the "tail", until their block
+        completes).  rows[name]: [B, >= max(n_new), dim] device tensors of the new
+        tokens' rows (k_tok, v_tok, gate and, for CSA, ki_tok); the first n_new[b]
+        of sequence b are used.  They are copied to their ring slots, then the blocks
+        they complete are compressed in one call.  Returns the new context lengths."""
+        if self.state is None:
+            raise RuntimeError("append needs a CacheState")
+        n_new = np.asarray(n_new, dtype=np.int64).reshape(-1)
+        slots = [self.state.slots(b, int(n_new[b])) for b in range(self.w.B)]
+        blk_begin, n_blk = self.state.append(n_new)
+        for name, dst in self.tok.items():
+            for b in range(self.w.B):
+                if n_new[b] == 0:
+                    continue
+                idx = torch.as_tensor(slots[b], device=dst.device)
+                dst[b].index_copy_(0, idx, rows[name][b, :int(n_new[b])].to(dst.dtype))
+        if n_blk > 0:
+            self.compress(torch.as_tensor(blk_begin, device=self.device), n_blk, stream)
+        return self.state.ctx.copy()
 
     def prefill_chunk(self, q, q_pos, qI=None, w_idx=None, stream=None):
         """Tq queries per sequence (their tokens and blocks already in the caches)."""
