@@ -163,7 +163,9 @@ ha_status csa_topk(const ha_params* p, const float* scores, int32_t n_cap,
  *   idx        : int32 [B, k]  CSA: attended entries (any order; entries < 0 or
  *                >= min(n_elig(t), n_cap) are ignored)
  *                NULL         HCA: every entry j < min(n_elig(t), n_cap)
- *   k_tok,v_tok: T [B, tok_cap, d]     window source, tok_cap >= n_win
+ *   k_tok,v_tok: T [B, tok_cap, d]     window source, tok_cap >= n_win; both
+ *                NULL: no window keys (a shard of a sequence that does not hold the
+ *                sequence's tail; tok_cap is then ignored)
  *   ctx_len    : int32 [B]   context length including the query token;
  *                <= 0 gives o = 0, lse = -inf for that sequence
  *   o          : T [B, H, d]           lse : float [B, H] or NULL
@@ -178,6 +180,21 @@ ha_status hybrid_attn_decode(const ha_params* p, const void* q, const void* ck, 
                              const void* v_tok, int32_t tok_cap, const int32_t* ctx_len,
                              void* o, float* lse, void* ws, size_t ws_bytes,
                              ha_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * hybrid_attn_merge -- combine attention results over disjoint key sets into the
+ * result over their union ([EP95] figure: one softmax over all keys; this is that
+ * softmax assembled from parts, e.g. from the shards of a sequence whose
+ * compressed entries are spread over several GPUs).  Per row and head:
+ *   LSE = log sum_s exp(lse_s),  o = sum_s exp(lse_s - LSE) o_s,
+ * parts with lse_s = -inf carry no weight; no part with a key gives o = 0,
+ * LSE = -inf.  The parts are added in part order (deterministic).
+ *   o_part : float [rows, S, H, d]     lse_part : float [rows, S, H]
+ *   o      : T [rows, H, d]            lse : float [rows, H] or NULL
+ * p supplies H, d and the type of o; 1 <= S <= 4096.
+ * ------------------------------------------------------------------------- */
+ha_status hybrid_attn_merge(const ha_params* p, int32_t rows, int32_t S, const float* o_part,
+                            const float* lse_part, void* o, float* lse, ha_stream_t stream);
 
 /* ---------------------------------------------------------------------------
  * hybrid_attn_prefill -- Tq queries per sequence at absolute positions q_pos,

@@ -57,6 +57,7 @@ _SIGS = {
                         _SZ, _P],
     "hybrid_attn_decode_static": [ctypes.POINTER(Params), _P, _P, _P, _I, _P, _P, _P, _I, _P, _P,
                                   _P, _P],
+    "hybrid_attn_merge": [ctypes.POINTER(Params), _I, _I, _P, _P, _P, _P, _P],
     "ha_workspace_size": [ctypes.POINTER(Params), _I, _I, _I, _I, ctypes.POINTER(ctypes.c_size_t)],
     "ha_device_error": [ctypes.POINTER(ctypes.c_int32), _I],
     "ha_selftest_wait_timeout": [_I, _P],
@@ -150,6 +151,11 @@ def hybrid_attn_decode(p, q, ck, cv, n_cap, idx, k_tok, v_tok, tok_cap, ctx_len,
     _call("hybrid_attn_decode", ctypes.byref(p), _ptr(q), _ptr(ck), _ptr(cv), n_cap, _ptr(idx),
           _ptr(k_tok), _ptr(v_tok), tok_cap, _ptr(ctx_len), _ptr(o), _ptr(lse), wp, wb,
           _stream(stream))
+
+
+def hybrid_attn_merge(p, rows, S, o_part, lse_part, o, lse=None, stream=None):
+    _call("hybrid_attn_merge", ctypes.byref(p), rows, S, _ptr(o_part), _ptr(lse_part), _ptr(o),
+          _ptr(lse), _stream(stream))
 
 
 def hybrid_attn_prefill(p, q, q_pos, Tq, ck, cv, n_cap, idx, k_tok, v_tok, tok_cap, o, lse=None,

@@ -341,15 +341,21 @@ ha_status hybrid_attn_decode(const ha_params* p, const void* q, const void* ck, 
   HA_PTR(ck);
   HA_PTR(cv);
   HA_OPT_PTR4(idx);
-  HA_PTR(k_tok);
-  HA_PTR(v_tok);
+  // both per-token caches NULL: no window keys (a shard without the sequence's tail)
+  const bool no_window = k_tok == nullptr && v_tok == nullptr;
+  if (!no_window) {
+    HA_PTR(k_tok);
+    HA_PTR(v_tok);
+    HA_REQUIRE(tok_cap >= p->n_win, HA_ERR_INVALID_ARG, "tok_cap = %d < n_win = %d", tok_cap,
+               p->n_win);
+  } else {
+    tok_cap = 0;
+  }
   HA_PTR4(ctx_len);
   HA_PTR(o);
   HA_OPT_PTR4(lse);
   HA_OPT_PTR(ws);
   HA_REQUIRE(n_cap >= 1, HA_ERR_INVALID_ARG, "n_cap = %d", n_cap);
-  HA_REQUIRE(tok_cap >= p->n_win, HA_ERR_INVALID_ARG, "tok_cap = %d < n_win = %d", tok_cap,
-             p->n_win);
   const bool tc = ha::attention_tc_supported(*p, n_cap, tok_cap);
   const ha::AttnPlan pl = attention_plan(p, p->B, n_cap, tok_cap, idx != nullptr, true);
   HA_REQUIRE(ws_bytes >= pl.ws_bytes && (pl.ws_bytes == 0 || ws != nullptr), HA_ERR_WORKSPACE,
@@ -365,6 +371,23 @@ ha_status hybrid_attn_decode(const ha_params* p, const void* q, const void* ck, 
   return cuda_status(ha::launch_attention_simt(*p, pl, 1, 1, q, ctx_len, ck, cv, n_cap, idx, k_tok,
                                                v_tok, tok_cap, o, lse, ws, (cudaStream_t)stream),
                      "decode launch");
+}
+
+ha_status hybrid_attn_merge(const ha_params* p, int32_t rows, int32_t S, const float* o_part,
+                            const float* lse_part, void* o, float* lse, ha_stream_t stream) {
+  g_last_error[0] = 0;
+  CallRange range("hybrid_attn_merge");
+  ha_status s = check_params(p, true, false);
+  if (s != HA_OK) return s;
+  HA_REQUIRE(rows >= 1, HA_ERR_INVALID_ARG, "rows = %d", rows);
+  HA_REQUIRE(S >= 1 && S <= 4096, HA_ERR_UNSUPPORTED, "S = %d (1..4096)", S);
+  HA_PTR(o_part);
+  HA_PTR4(lse_part);
+  HA_PTR(o);
+  HA_OPT_PTR4(lse);
+  return cuda_status(ha::launch_attn_merge(*p, rows, S, o_part, lse_part, o, lse,
+                                           (cudaStream_t)stream),
+                     "merge launch");
 }
 
 ha_status hybrid_attn_prefill(const ha_params* p, const void* q, const int32_t* q_pos,

@@ -60,7 +60,7 @@ __global__ void __launch_bounds__(kThreads) attn_simt(AttnArgs a) {
 
   const int ne = t >= 0 ? n_eligible(t, a.n_win, a.m, a.elig, a.n_cap) : 0;
   const int n_c = a.idx ? a.k : ne;
-  const int n_w = t >= 0 ? min(a.n_win, t + 1) : 0;
+  const int n_w = (t >= 0 && a.k_tok != nullptr) ? min(a.n_win, t + 1) : 0;   // null: no window
   const int n_keys = n_c + n_w;
   const int s_lo = split * a.keys_per_split;
   const int s_hi = min(n_keys, s_lo + a.keys_per_split);

@@ -121,7 +121,7 @@ __device__ __forceinline__ void item_tail(const TcArgs& a, Item& x) {
   x.t = a.decode ? a.pos[x.b] - 1 : a.pos[x.r];
   x.ne = x.t >= 0 ? n_eligible(x.t, a.n_win, a.m, a.elig, a.n_cap) : 0;
   x.n_c = a.idx ? a.k : x.ne;
-  x.n_w = x.t >= 0 ? min(a.n_win, x.t + 1) : 0;
+  x.n_w = (x.t >= 0 && a.k_tok != nullptr) ? min(a.n_win, x.t + 1) : 0;   // null: no window
   x.hi = min(x.n_c + x.n_w, x.lo + a.kps);
   const int n = x.hi - x.lo;
   x.nt = n > 0 ? (n + kTile - 1) / kTile : 1;
