@@ -4,14 +4,19 @@
 // softmax-gated sum is the formula this library fixes).  K, V and, for CSA, the
 // indexer keys are compressed with the same gates.
 //
-// HBM-bound streaming kernel: every thread owns one 16-byte chunk of one output
-// row and walks the block's tokens with 128-bit read-only loads; consecutive
-// threads read consecutive chunks of the same token row, so each warp issues
-// fully coalesced 512-byte requests.  Accumulation is float32 in token order.
-//   m <= 16 : one thread per (block, chunk) walks all m tokens.
-//   m  > 16 : the block's tokens are split into G = min(8, ceil(m/8)) contiguous
-//             groups; the G partial sums of a chunk are added in group order
-//             through shared memory, so the result does not depend on scheduling.
+// HBM-bound streaming kernel: every thread owns 16-byte chunks of output rows and
+// walks the block's tokens with 128-bit read-only loads; consecutive threads read
+// consecutive chunks of the same token row, so each warp issues fully coalesced
+// 512-byte requests.  Accumulation is float32 in token order.
+//   m <= 16 : one thread per (block, chunk) walks all m tokens; each thread keeps
+//             the loads of kItems such items in flight (m = 4 is compiled apart,
+//             with fewer registers).
+//   m  > 16 : the block's tokens are split into G = min(8, ceil(m/16)) contiguous
+//             groups whose loads are all issued at once; the G partial sums of a
+//             chunk are added in group order through shared memory, so the result
+//             does not depend on scheduling.
+// Ring slots: the block's first token slot is computed once per block; the next
+// slots follow by one increment and at most one wrap (m <= tok_cap).
 #include "common.cuh"
 #include "kernels.h"
 
@@ -38,74 +43,115 @@ __device__ __forceinline__ int first_block(const CompressArgs& a, int b) {
   return (c > 0 && c % a.m == 0) ? c / a.m - 1 : -1;
 }
 
-template <typename T>
-__device__ __forceinline__ void locate(const CompressArgs& a, int c, int& tsr, int& chunk) {
-  tsr = 0;
-  chunk = c;
-  while (tsr + 1 < a.n_tensors && chunk >= a.chunks[tsr]) { chunk -= a.chunks[tsr]; ++tsr; }
+// Tensor of chunk c of the concatenated rows (K | V | indexer keys), by selects
+// rather than indexing the argument arrays (which would copy them to local memory).
+struct ChunkRef {
+  const void* src;
+  void* dst;
+  int chunk, row_chunks;
+};
+__device__ __forceinline__ ChunkRef chunk_ref(const CompressArgs& a, int c) {
+  ChunkRef r;
+  if (c < a.chunks[0]) {
+    r.src = a.src[0]; r.dst = a.dst[0]; r.chunk = c; r.row_chunks = a.chunks[0];
+  } else if (c < a.chunks[0] + a.chunks[1]) {
+    r.src = a.src[1]; r.dst = a.dst[1]; r.chunk = c - a.chunks[0]; r.row_chunks = a.chunks[1];
+  } else {
+    r.src = a.src[2]; r.dst = a.dst[2]; r.chunk = c - a.chunks[0] - a.chunks[1];
+    r.row_chunks = a.chunks[2];
+  }
+  return r;
 }
 
-// Softmax weights of one block's gates, computed by one thread (m small).
-template <typename T>
+// Slot of the first token of block j in the per-token cache of capacity tok_cap.
+__device__ __forceinline__ int block_slot(int j, int m, int tok_cap) {
+  return int((unsigned long long)j * unsigned(m) % unsigned(tok_cap));
+}
+
+constexpr int kItems = 2;        // (block, chunk) items per thread in flight
+
+// One item of compress_small_m: the loads of its m rows and gates.
+template <typename T, int MM>
+struct SmallItem {
+  uint4 raw[MM];
+  float g[MM];
+  T* dst;
+  bool live;
+};
+
+template <typename T, int M>     // M > 0: block size fixed at compile time
 __global__ void __launch_bounds__(256) compress_small_m(CompressArgs a) {
   constexpr int V = Elem<T>::kVec;
+  constexpr int MM = M > 0 ? M : 16;
+  const int m = M > 0 ? M : a.m;
   pdl_wait_then_release();
   const int total_chunks = a.chunks[0] + a.chunks[1] + a.chunks[2];
   const long long n_items = (long long)a.B * a.n_blk * total_chunks;
-  for (long long it = blockIdx.x * (long long)blockDim.x + threadIdx.x; it < n_items;
-       it += (long long)gridDim.x * blockDim.x) {
-    const int c = int(it % total_chunks);
-    const long long task = it / total_chunks;
-    const int b = int(task / a.n_blk);
-    const int fb = first_block(a, b);
-    const int j = fb < 0 ? -1 : fb + int(task % a.n_blk);
-    if (j < 0 || j >= a.n_cap) continue;
-    int tsr, chunk;
-    locate<T>(a, c, tsr, chunk);
-    const int row_elems = a.chunks[tsr] * V;
-    // the block's rows and gates are loaded together (neither depends on the other)
-    const T* src = static_cast<const T*>(a.src[tsr]);
-    uint4 raw[16];
-    float g[16];
+  const long long stride = (long long)gridDim.x * blockDim.x;
+  for (long long base = blockIdx.x * (long long)blockDim.x + threadIdx.x; base < n_items;
+       base += kItems * stride) {
+    SmallItem<T, MM> itm[kItems];
+    // every item's rows and gates are requested before any of them is used
 #pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      if (i < a.m) {
-        const long long u = (long long)j * a.m + i;
-        const long long slot = (long long)b * a.tok_cap + u % a.tok_cap;
-        raw[i] = ld16(src + slot * row_elems + chunk * V);
-        g[i] = a.gate[slot];
+    for (int k = 0; k < kItems; ++k) {
+      const long long it = base + k * stride;
+      itm[k].live = false;
+      if (it >= n_items) continue;
+      const int c = int(it % total_chunks);
+      const long long task = it / total_chunks;
+      const int b = int(task / a.n_blk);
+      const int fb = first_block(a, b);
+      const int j = fb < 0 ? -1 : fb + int(task % a.n_blk);
+      if (j < 0 || j >= a.n_cap) continue;
+      const ChunkRef r = chunk_ref(a, c);
+      const long long rowb = (long long)r.row_chunks * V;
+      const T* src = static_cast<const T*>(r.src) + (long long)b * a.tok_cap * rowb + r.chunk * V;
+      const float* gate = a.gate + (long long)b * a.tok_cap;
+      int slot = block_slot(j, m, a.tok_cap);
+#pragma unroll
+      for (int i = 0; i < MM; ++i) {
+        if (i < m) {
+          itm[k].raw[i] = ld16(src + slot * rowb);
+          itm[k].g[i] = gate[slot];
+          if (++slot == a.tok_cap) slot = 0;
+        }
       }
+      itm[k].dst = static_cast<T*>(r.dst) + ((long long)b * a.n_cap + j) * rowb + r.chunk * V;
+      itm[k].live = true;
     }
-    float gmax = -INFINITY;
 #pragma unroll
-    for (int i = 0; i < 16; ++i)
-      if (i < a.m) gmax = fmaxf(gmax, g[i]);
-    float den = 0.f;
+    for (int k = 0; k < kItems; ++k) {
+      if (!itm[k].live) continue;
+      float gmax = -INFINITY;
 #pragma unroll
-    for (int i = 0; i < 16; ++i)
-      if (i < a.m) { g[i] = expf(g[i] - gmax); den += g[i]; }
-    const float inv = 1.f / den;
-    float acc[V];
+      for (int i = 0; i < MM; ++i)
+        if (i < m) gmax = fmaxf(gmax, itm[k].g[i]);
+      float den = 0.f;
 #pragma unroll
-    for (int e = 0; e < V; ++e) acc[e] = 0.f;
+      for (int i = 0; i < MM; ++i)
+        if (i < m) { itm[k].g[i] = expf(itm[k].g[i] - gmax); den += itm[k].g[i]; }
+      const float inv = 1.f / den;
+      float acc[V];
 #pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      if (i < a.m) {
-        float f[V];
-        unpack(raw[i], f);
-        const float al = g[i] * inv;
+      for (int e = 0; e < V; ++e) acc[e] = 0.f;
 #pragma unroll
-        for (int e = 0; e < V; ++e) acc[e] = fmaf(al, f[e], acc[e]);
+      for (int i = 0; i < MM; ++i) {
+        if (i < m) {
+          float f[V];
+          unpack(itm[k].raw[i], f);
+          const float al = itm[k].g[i] * inv;
+#pragma unroll
+          for (int e = 0; e < V; ++e) acc[e] = fmaf(al, f[e], acc[e]);
+        }
       }
+      st16(itm[k].dst, pack(acc));
     }
-    T* dst = static_cast<T*>(a.dst[tsr]) + ((long long)b * a.n_cap + j) * row_elems;
-    st16(dst + chunk * V, pack(acc));
   }
 }
 
 // CTA = (block task, slice of kSlice chunks) x G token groups.
-constexpr int kSlice = 64;
-constexpr int kBatch = 8;        // loads in flight per thread
+constexpr int kSlice = 32;
+constexpr int kBatch = 16;       // loads in flight per thread (a whole token group)
 constexpr int kMaxGroups = 8;
 
 __host__ __device__ inline int n_groups(int m) {
@@ -114,7 +160,7 @@ __host__ __device__ inline int n_groups(int m) {
 }
 
 template <typename T>
-__global__ void __launch_bounds__(512) compress_large_m(CompressArgs a) {
+__global__ void __launch_bounds__(kMaxGroups * kSlice) compress_large_m(CompressArgs a) {
   constexpr int V = Elem<T>::kVec;
   pdl_wait_then_release();
   extern __shared__ float sm[];                    // alpha[m] | partial[G][kSlice][V]
@@ -129,32 +175,48 @@ __global__ void __launch_bounds__(512) compress_large_m(CompressArgs a) {
   if (j < 0 || j >= a.n_cap) return;                // uniform over the CTA
   const int lane_c = threadIdx.x % kSlice;          // chunk within the slice
   const int grp = threadIdx.x / kSlice;             // token group
-  const long long base_u = (long long)j * a.m;
+  const int slot0 = block_slot(j, a.m, a.tok_cap);  // slot of the block's first token
 
-  // the first batch of this thread's rows is requested before the gate softmax
+  // this thread's rows: the first kBatch of its group are requested before the
+  // gate softmax
   const int c = blockIdx.y * kSlice + lane_c;       // chunk over all tensors
   const int total_chunks = a.chunks[0] + a.chunks[1] + a.chunks[2];
-  int tsr = 0, chunk = 0, row_elems = 0;
-  const T* src = nullptr;
   const int i_beg = grp * per_group, i_end = min(a.m, (grp + 1) * per_group);
+  const T* src = nullptr;
+  long long rowb = 0;
+  ChunkRef r{};
   uint4 raw[kBatch];
-  if (c < total_chunks) {
-    locate<T>(a, c, tsr, chunk);
-    row_elems = a.chunks[tsr] * V;
-    src = static_cast<const T*>(a.src[tsr]) + (long long)b * a.tok_cap * row_elems;
+  auto load_batch = [&](int i0) {
+    int slot = slot0 + i0;
+    if (slot >= a.tok_cap) slot -= a.tok_cap;
 #pragma unroll
-    for (int i = 0; i < kBatch; ++i)
-      if (i_beg + i < i_end) raw[i] = ld16(src + ((base_u + i_beg + i) % a.tok_cap) * row_elems + chunk * V);
+    for (int i = 0; i < kBatch; ++i) {
+      if (i0 + i < i_end) {
+        raw[i] = ld16(src + slot * rowb);
+        if (++slot == a.tok_cap) slot = 0;
+      }
+    }
+  };
+  if (c < total_chunks) {
+    r = chunk_ref(a, c);
+    rowb = (long long)r.row_chunks * V;
+    src = static_cast<const T*>(r.src) + (long long)b * a.tok_cap * rowb + r.chunk * V;
+    load_batch(i_beg);
   }
   // gate softmax of this block (warp 0, fixed order)
   if (threadIdx.x < 32) {
+    const float* gate = a.gate + (long long)b * a.tok_cap;
     float mx = -INFINITY;
-    for (int i = threadIdx.x; i < a.m; i += 32)
-      mx = fmaxf(mx, a.gate[(long long)b * a.tok_cap + (base_u + i) % a.tok_cap]);
+    for (int i = threadIdx.x; i < a.m; i += 32) {
+      int slot = slot0 + i;
+      if (slot >= a.tok_cap) slot -= a.tok_cap;
+      alpha[i] = gate[slot];
+      mx = fmaxf(mx, alpha[i]);
+    }
     mx = warp_max(mx);
     float den = 0.f;
     for (int i = threadIdx.x; i < a.m; i += 32) {
-      const float e = expf(a.gate[(long long)b * a.tok_cap + (base_u + i) % a.tok_cap] - mx);
+      const float e = expf(alpha[i] - mx);
       alpha[i] = e;
       den += e;
     }
@@ -170,11 +232,7 @@ __global__ void __launch_bounds__(512) compress_large_m(CompressArgs a) {
   for (int e = 0; e < V; ++e) acc[e] = 0.f;
   if (c < total_chunks) {
     for (int i0 = i_beg; i0 < i_end; i0 += kBatch) {
-      if (i0 != i_beg) {
-#pragma unroll
-        for (int i = 0; i < kBatch; ++i)
-          if (i0 + i < i_end) raw[i] = ld16(src + ((base_u + i0 + i) % a.tok_cap) * row_elems + chunk * V);
-      }
+      if (i0 != i_beg) load_batch(i0);
 #pragma unroll
       for (int i = 0; i < kBatch; ++i) {
         if (i0 + i < i_end) {
@@ -195,8 +253,8 @@ __global__ void __launch_bounds__(512) compress_large_m(CompressArgs a) {
 #pragma unroll
       for (int e = 0; e < V; ++e) acc[e] += part[(g2 * kSlice + lane_c) * V + e];
     }
-    T* dst = static_cast<T*>(a.dst[tsr]) + ((long long)b * a.n_cap + j) * row_elems;
-    st16(dst + chunk * V, pack(acc));
+    T* dst = static_cast<T*>(r.dst) + ((long long)b * a.n_cap + j) * rowb;
+    st16(dst + r.chunk * V, pack(acc));
   }
 }
 
@@ -205,9 +263,10 @@ cudaError_t launch(const CompressArgs& a, cudaStream_t st) {
   const int total_chunks = a.chunks[0] + a.chunks[1] + a.chunks[2];
   if (a.m <= 16) {
     const long long n_items = (long long)a.B * a.n_blk * total_chunks;
-    const long long want = (n_items + 255) / 256;
+    const long long want = (n_items + 256 * kItems - 1) / (256 * kItems);
     const int grid = int(want < 148LL * 32 ? want : 148LL * 32);
-    return launch_pdl(compress_small_m<T>, dim3(grid), dim3(256), 0, st, 1, a);
+    if (a.m == 4) return launch_pdl(compress_small_m<T, 4>, dim3(grid), dim3(256), 0, st, 1, a);
+    return launch_pdl(compress_small_m<T, 0>, dim3(grid), dim3(256), 0, st, 1, a);
   } else {
     const int G = n_groups(a.m);
     const dim3 grid(a.B * a.n_blk, (total_chunks + kSlice - 1) / kSlice);
