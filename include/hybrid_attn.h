@@ -76,6 +76,21 @@ typedef enum {
 } ha_status;
 
 typedef enum { HA_F32 = 0, HA_BF16 = 1 } ha_dtype;
+
+/* Storage formats of the deployed model ([V4-notes] §8), bit flags of
+ * ha_params.fmt; both need dtype HA_BF16.
+ *   HA_FMT_IDX4: the Lightning Indexer computes in FP4 and keeps its scores in
+ *     BF16.  Compressed indexer keys (cki) are rows of 80 bytes: d_I = 128
+ *     e2m1 codes, two per byte (element 2i in the low nibble), then 8 e4m3fn
+ *     scales (one per 16 consecutive elements), then 8 unused bytes; element
+ *     value = code * scale.  scale = e4m3(amax / 6) of its 16 elements, code =
+ *     e2m1(x / scale), both rounded to nearest even (codes saturate at 6), the
+ *     divisions in float32; an all-zero group has scale 0 and codes 0.  The
+ *     indexer's queries (q_idx, still given in bfloat16) are quantized the
+ *     same way inside the indexer.  Index scores are bfloat16 (the float32 sum
+ *     rounded to nearest even): csa_index_scores writes them and csa_topk reads
+ *     them.  Needs H_I = 64 and d_I = 128. */
+enum { HA_FMT_IDX4 = 2 };
 typedef enum { HA_ELIG_DISJOINT = 0, HA_ELIG_OVERLAP = 1 } ha_elig;
 typedef enum { HA_OP_TOPK = 0, HA_OP_DECODE = 1, HA_OP_PREFILL = 2, HA_OP_DECODE_STEP = 3 } ha_op;
 
@@ -94,6 +109,7 @@ typedef struct {
   int32_t dtype; /* ha_dtype of every T array                                */
   int32_t elig;  /* ha_elig                                                  */
   float scale;   /* softmax scale of the attention                           */
+  int32_t fmt;   /* storage-format bits (HA_FMT_*), 0 = plain dtype storage  */
 } ha_params;
 
 /* ---------------------------------------------------------------------------
@@ -119,6 +135,8 @@ ha_status hca_compress_kv(const ha_params* p, const void* k_tok, const void* v_t
  * own).  As hca_compress_kv, plus the indexer keys, compressed with the same
  * gates:
  *   ki_tok : T [B, tok_cap, d_I]   cki : T [B, n_cap, d_I]
+ * Under HA_FMT_IDX4 cki holds the 80-byte FP4 rows [B, n_cap, 80] of the
+ * compressed indexer keys (m <= 16).
  * ------------------------------------------------------------------------- */
 ha_status csa_compress_kv(const ha_params* p, const void* k_tok, const void* v_tok,
                           const void* ki_tok, const float* gate, int32_t tok_cap,
@@ -132,17 +150,20 @@ ha_status csa_compress_kv(const ha_params* p, const void* k_tok, const void* v_t
  *   q_idx  : T [B, Tq, H_I, d_I]      w_idx : float [B, Tq, H_I]
  *   cki    : T [B, n_cap, d_I]        q_pos : int32 [B, Tq] absolute positions
  *   scores : float [B, Tq, n_cap]     written for j < min(n_elig(q_pos), n_cap)
- *            only; the rest of each row is left untouched.
+ *            only; the rest of each row is left untouched.  bfloat16 [B, Tq,
+ *            n_cap] under HA_FMT_IDX4, where cki holds 80-byte FP4 rows
+ *            [B, n_cap, 80] and q_idx is quantized to FP4 inside the call.
  * ------------------------------------------------------------------------- */
 ha_status csa_index_scores(const ha_params* p, const void* q_idx, const float* w_idx,
                            const void* cki, int32_t n_cap, const int32_t* q_pos, int32_t Tq,
-                           float* scores, ha_stream_t stream);
+                           void* scores, ha_stream_t stream);
 
 /* ---------------------------------------------------------------------------
  * csa_topk -- top-k selection of compressed entries ([V4-notes] §5.3: k = 512
  * for V4-Flash, 1024 for V4-Pro).  Per row (b, t) over the n = min(n_elig(t),
  * n_cap) eligible scores: the k best by (score descending, index ascending),
- * NaN ranked as -inf; all n when n <= k.  Written in ascending index order,
+ * NaN ranked as -inf; all n when n <= k.  scores as written by csa_index_scores
+ * (float32, or bfloat16 under HA_FMT_IDX4).  Written in ascending index order,
  * padded with -1:
  *   idx : int32 [B, Tq, k]
  *   ws  : device workspace of ha_workspace_size(p, HA_OP_TOPK, Tq, n_cap) bytes
@@ -150,7 +171,7 @@ ha_status csa_index_scores(const ha_params* p, const void* q_idx, const float* w
  *         into segments whose candidate lists go through ws).
  * n_cap above 41,943,040 (= 40,960 x 1,024) returns HA_ERR_UNSUPPORTED.
  * ------------------------------------------------------------------------- */
-ha_status csa_topk(const ha_params* p, const float* scores, int32_t n_cap,
+ha_status csa_topk(const ha_params* p, const void* scores, int32_t n_cap,
                    const int32_t* q_pos, int32_t Tq, int32_t* idx, void* ws, size_t ws_bytes,
                    ha_stream_t stream);
 
@@ -232,7 +253,7 @@ ha_status hybrid_attn_prefill(const ha_params* p, const void* q, const int32_t* 
  *   k_tok, v_tok : T [B, tok_cap, d]    ki_tok : T [B, tok_cap, d_I]
  *   gate   : float [B, tok_cap]  ctx_len : int32 [B]  (tok_cap >= max(n_win, m))
  *   ck, cv : T [B, n_cap, d]     cki : T [B, n_cap, d_I]
- *   scores : float [B, n_cap]    idx : int32 [B, k]
+ *   scores : float [B, n_cap] (bfloat16 under HA_FMT_IDX4)    idx : int32 [B, k]
  *   o      : T [B, H, d]         lse : float [B, H] or NULL
  *   ws     : ha_workspace_size(p, HA_OP_DECODE_STEP, 1, n_cap, 1) bytes
  * ------------------------------------------------------------------------- */
@@ -240,7 +261,7 @@ ha_status csa_decode_step(const ha_params* p, const void* q, const void* q_idx,
                           const float* w_idx, const void* k_tok, const void* v_tok,
                           const void* ki_tok, const float* gate, int32_t tok_cap,
                           const int32_t* ctx_len, void* ck, void* cv, void* cki, int32_t n_cap,
-                          float* scores, int32_t* idx, void* o, float* lse, void* ws,
+                          void* scores, int32_t* idx, void* o, float* lse, void* ws,
                           size_t ws_bytes, ha_stream_t stream);
 
 /* ---------------------------------------------------------------------------

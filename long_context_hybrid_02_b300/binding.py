@@ -32,11 +32,16 @@ class Params(ctypes.Structure):
     _fields_ = [("B", ctypes.c_int32), ("H", ctypes.c_int32), ("d", ctypes.c_int32),
                 ("n_win", ctypes.c_int32), ("m", ctypes.c_int32), ("k", ctypes.c_int32),
                 ("H_I", ctypes.c_int32), ("d_I", ctypes.c_int32), ("dtype", ctypes.c_int32),
-                ("elig", ctypes.c_int32), ("scale", ctypes.c_float)]
+                ("elig", ctypes.c_int32), ("scale", ctypes.c_float), ("fmt", ctypes.c_int32)]
 
 
-def make_params(B, H, d, n_win, m, k=1, H_I=1, d_I=8, dtype=BF16, elig=ELIG_DISJOINT, scale=0.0):
-    return Params(B, H, d, n_win, m, k, H_I, d_I, dtype, elig, scale)
+FMT_IDX4 = 2           # FP4 indexer keys and queries, bfloat16 index scores
+IDX4_ROW_BYTES = 80    # one FP4 indexer key row (d_I = 128)
+
+
+def make_params(B, H, d, n_win, m, k=1, H_I=1, d_I=8, dtype=BF16, elig=ELIG_DISJOINT, scale=0.0,
+                fmt=0):
+    return Params(B, H, d, n_win, m, k, H_I, d_I, dtype, elig, scale, fmt)
 
 
 _P = ctypes.c_void_p

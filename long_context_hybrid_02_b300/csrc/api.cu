@@ -130,6 +130,12 @@ ha_status check_params(const ha_params* p, bool need_attn, bool need_index) {
     HA_REQUIRE(p->H >= 1 && p->H <= 256, HA_ERR_UNSUPPORTED, "H = %d (1..256)", p->H);
     HA_REQUIRE(isfinite(p->scale), HA_ERR_INVALID_ARG, "scale is not finite");
   }
+  HA_REQUIRE((p->fmt & ~HA_FMT_IDX4) == 0, HA_ERR_INVALID_ARG, "fmt = %d", p->fmt);
+  HA_REQUIRE(p->fmt == 0 || p->dtype == HA_BF16, HA_ERR_UNSUPPORTED,
+             "storage formats need bfloat16 (fmt = %d)", p->fmt);
+  if ((p->fmt & HA_FMT_IDX4) && need_index)
+    HA_REQUIRE(p->H_I == 64 && p->d_I == 128, HA_ERR_UNSUPPORTED,
+               "the FP4 indexer needs H_I = 64 and d_I = 128 (got %d, %d)", p->H_I, p->d_I);
   if (need_index) {
     HA_REQUIRE(p->H_I >= 1 && p->H_I <= 128, HA_ERR_UNSUPPORTED, "H_I = %d (1..128)", p->H_I);
     HA_REQUIRE(p->d_I >= 8 && p->d_I <= 512 && p->d_I % 8 == 0, HA_ERR_UNSUPPORTED,
@@ -173,6 +179,8 @@ ha_status compress_common(const ha_params* p, int n_tensors, const void* const* 
   HA_PTR4(gate);
   HA_PTR4(blk_begin);
   HA_REQUIRE(tok_cap >= p->m, HA_ERR_INVALID_ARG, "tok_cap = %d < m = %d", tok_cap, p->m);
+  HA_REQUIRE(!(csa && (p->fmt & HA_FMT_IDX4)) || p->m <= 16, HA_ERR_UNSUPPORTED,
+             "FP4 indexer keys need m <= 16 (m = %d)", p->m);
   HA_REQUIRE(n_blk >= 0, HA_ERR_INVALID_ARG, "n_blk = %d", n_blk);
   HA_REQUIRE(n_cap >= 1, HA_ERR_INVALID_ARG, "n_cap = %d", n_cap);
   HA_REQUIRE((long long)p->B * n_blk <= 0x7fffffffLL, HA_ERR_UNSUPPORTED, "B * n_blk too large");
@@ -226,7 +234,7 @@ void ha::set_last_error(const char* msg) {
 
 extern "C" {
 
-int32_t ha_abi_version(void) { return 2; }
+int32_t ha_abi_version(void) { return 3; }
 
 uint64_t ha_launch_count(void) { return ha::launch_count(); }
 
@@ -274,7 +282,7 @@ ha_status csa_compress_kv(const ha_params* p, const void* k_tok, const void* v_t
 
 ha_status csa_index_scores(const ha_params* p, const void* q_idx, const float* w_idx,
                            const void* cki, int32_t n_cap, const int32_t* q_pos, int32_t Tq,
-                           float* scores, ha_stream_t stream) {
+                           void* scores, ha_stream_t stream) {
   g_last_error[0] = 0;
   CallRange range("csa_index_scores");
   ha_status s = check_params(p, false, true);
@@ -294,12 +302,12 @@ ha_status csa_index_scores(const ha_params* p, const void* q_idx, const float* w
                                                   err, (cudaStream_t)stream),
                        "index launch (tensor cores)");
   }
-  return cuda_status(ha::launch_index_scores_simt(*p, q_idx, w_idx, cki, n_cap, q_pos, Tq, scores,
-                                                  (cudaStream_t)stream),
+  return cuda_status(ha::launch_index_scores_simt(*p, q_idx, w_idx, cki, n_cap, q_pos, Tq,
+                                                  static_cast<float*>(scores), (cudaStream_t)stream),
                      "index launch");
 }
 
-ha_status csa_topk(const ha_params* p, const float* scores, int32_t n_cap, const int32_t* q_pos,
+ha_status csa_topk(const ha_params* p, const void* scores, int32_t n_cap, const int32_t* q_pos,
                    int32_t Tq, int32_t* idx, void* ws, size_t ws_bytes, ha_stream_t stream) {
   g_last_error[0] = 0;
   CallRange range("csa_topk");
@@ -439,7 +447,7 @@ ha_status csa_decode_step(const ha_params* p, const void* q, const void* q_idx,
                           const float* w_idx, const void* k_tok, const void* v_tok,
                           const void* ki_tok, const float* gate, int32_t tok_cap,
                           const int32_t* ctx_len, void* ck, void* cv, void* cki, int32_t n_cap,
-                          float* scores, int32_t* idx, void* o, float* lse, void* ws,
+                          void* scores, int32_t* idx, void* o, float* lse, void* ws,
                           size_t ws_bytes, ha_stream_t stream) {
   g_last_error[0] = 0;
   CallRange range("csa_decode_step");
@@ -484,7 +492,8 @@ ha_status csa_decode_step(const ha_params* p, const void* q, const void* q_idx,
     si.wait_last = overlap ? 1 : 0;
     e = ha::launch_index_scores_tc(*p, q_idx, w_idx, cki, n_cap, ctx_len, 1, scores, err, st, si);
   } else {
-    e = ha::launch_index_scores_simt(*p, q_idx, w_idx, cki, n_cap, ctx_len, 1, scores, st, si);
+    e = ha::launch_index_scores_simt(*p, q_idx, w_idx, cki, n_cap, ctx_len, 1,
+                                     static_cast<float*>(scores), st, si);
   }
   if (e != cudaSuccess) return cuda_status(e, "step: index launch");
   ha::StepOpts sk;

@@ -18,6 +18,7 @@
 // Ring slots: the block's first token slot is computed once per block; the next
 // slots follow by one increment and at most one wrap (m <= tok_cap).
 #include "common.cuh"
+#include "fp4.cuh"
 #include "kernels.h"
 
 namespace ha {
@@ -32,6 +33,7 @@ struct CompressArgs {
   const int32_t* blk_begin;
   const int32_t* ctx_len;   // non-null: the block the newest token completes (n_blk = 1)
   int B, n_blk, m, tok_cap, n_cap;
+  int fp4_third;            // the third tensor (indexer keys) is written in the FP4 format
 };
 
 // First block to compress for sequence b: blk_begin[b], or the block completed by
@@ -48,17 +50,19 @@ __device__ __forceinline__ int first_block(const CompressArgs& a, int b) {
 struct ChunkRef {
   const void* src;
   void* dst;
-  int chunk, row_chunks;
+  int chunk, row_chunks, tensor;
 };
 __device__ __forceinline__ ChunkRef chunk_ref(const CompressArgs& a, int c) {
   ChunkRef r;
   if (c < a.chunks[0]) {
-    r.src = a.src[0]; r.dst = a.dst[0]; r.chunk = c; r.row_chunks = a.chunks[0];
+    r.src = a.src[0]; r.dst = a.dst[0]; r.chunk = c; r.row_chunks = a.chunks[0]; r.tensor = 0;
   } else if (c < a.chunks[0] + a.chunks[1]) {
     r.src = a.src[1]; r.dst = a.dst[1]; r.chunk = c - a.chunks[0]; r.row_chunks = a.chunks[1];
+    r.tensor = 1;
   } else {
     r.src = a.src[2]; r.dst = a.dst[2]; r.chunk = c - a.chunks[0] - a.chunks[1];
     r.row_chunks = a.chunks[2];
+    r.tensor = 2;
   }
   return r;
 }
@@ -76,6 +80,8 @@ struct SmallItem {
   uint4 raw[MM];
   float g[MM];
   T* dst;
+  unsigned char* row4;   // FP4 indexer-key row (fp4_third), else null
+  int chunk;
   bool live;
 };
 
@@ -96,6 +102,7 @@ __global__ void __launch_bounds__(256) compress_small_m(CompressArgs a) {
     for (int k = 0; k < kItems; ++k) {
       const long long it = base + k * stride;
       itm[k].live = false;
+      itm[k].row4 = nullptr;
       if (it >= n_items) continue;
       const int c = int(it % total_chunks);
       const long long task = it / total_chunks;
@@ -117,11 +124,18 @@ __global__ void __launch_bounds__(256) compress_small_m(CompressArgs a) {
         }
       }
       itm[k].dst = static_cast<T*>(r.dst) + ((long long)b * a.n_cap + j) * rowb + r.chunk * V;
+      if (a.fp4_third && r.tensor == 2)
+        itm[k].row4 = static_cast<unsigned char*>(a.dst[2]) +
+                      ((long long)b * a.n_cap + j) * fp4::kRowBytes;
+      itm[k].chunk = r.chunk;
       itm[k].live = true;
     }
 #pragma unroll
     for (int k = 0; k < kItems; ++k) {
-      if (!itm[k].live) continue;
+      float acc[V];
+#pragma unroll
+      for (int e = 0; e < V; ++e) acc[e] = 0.f;
+      if (itm[k].live) {
       float gmax = -INFINITY;
 #pragma unroll
       for (int i = 0; i < MM; ++i)
@@ -131,9 +145,6 @@ __global__ void __launch_bounds__(256) compress_small_m(CompressArgs a) {
       for (int i = 0; i < MM; ++i)
         if (i < m) { itm[k].g[i] = expf(itm[k].g[i] - gmax); den += itm[k].g[i]; }
       const float inv = 1.f / den;
-      float acc[V];
-#pragma unroll
-      for (int e = 0; e < V; ++e) acc[e] = 0.f;
 #pragma unroll
       for (int i = 0; i < MM; ++i) {
         if (i < m) {
@@ -144,7 +155,30 @@ __global__ void __launch_bounds__(256) compress_small_m(CompressArgs a) {
           for (int e = 0; e < V; ++e) acc[e] = fmaf(al, f[e], acc[e]);
         }
       }
-      st16(itm[k].dst, pack(acc));
+      }
+      if constexpr (V == 8) {
+        if (a.fp4_third) {
+          // FP4 indexer keys: a 16-element group is the chunk pair (2g, 2g + 1), held
+          // by lanes (2l, 2l + 1) (items and chunks alternate parity alike, and both
+          // lanes of a pair are live or not together); the pair's amax gives the scale
+          const int lane = threadIdx.x & 31;
+          const bool q4 = itm[k].live && itm[k].row4 != nullptr;
+          float amax = 0.f;
+          if (q4)
+#pragma unroll
+            for (int e = 0; e < V; ++e) amax = fmaxf(amax, fabsf(acc[e]));
+          amax = fmaxf(amax, __shfl_xor_sync(3u << (lane & ~1), amax, 1));
+          if (q4) {
+            uint32_t sbyte;
+            float sv;
+            const uint32_t codes = fp4::quantize8(acc, amax, sbyte, sv);
+            *reinterpret_cast<uint32_t*>(itm[k].row4 + 4 * itm[k].chunk) = codes;
+            if ((itm[k].chunk & 1) == 0) itm[k].row4[64 + itm[k].chunk / 2] = uint8_t(sbyte);
+            continue;
+          }
+        }
+      }
+      if (itm[k].live) st16(itm[k].dst, pack(acc));
     }
   }
 }
@@ -285,6 +319,7 @@ cudaError_t launch_compress(const ha_params& p, int n_tensors, const void* const
                             cudaStream_t st, const StepOpts& so) {
   CompressArgs a{};
   a.ctx_len = so.ctx_len;
+  a.fp4_third = (p.fmt & HA_FMT_IDX4) && n_tensors == 3 ? 1 : 0;
   const int V = p.dtype == HA_BF16 ? 8 : 4;
   for (int i = 0; i < 3; ++i) {
     a.src[i] = i < n_tensors ? src[i] : nullptr;

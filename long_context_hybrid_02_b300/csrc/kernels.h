@@ -47,15 +47,16 @@ cudaError_t launch_index_scores_simt(const ha_params& p, const void* q_idx, cons
 
 // indexer_tc.cu: tcgen05 indexer for bf16, H_I = 64, d_I = 128.
 bool index_scores_tc_supported(const ha_params& p, const void* q_idx, const void* cki);
+// Scores are float32, or bfloat16 when p.fmt has HA_FMT_IDX4 (the FP4 indexer).
 cudaError_t launch_index_scores_tc(const ha_params& p, const void* q_idx, const float* w_idx,
                                    const void* cki, int n_cap, const int32_t* q_pos, int Tq,
-                                   float* scores, int* err, cudaStream_t st,
+                                   void* scores, int* err, cudaStream_t st,
                                    const StepOpts& so = StepOpts());
 
 // topk.cu
 size_t topk_workspace_bytes(const ha_params& p, int Tq, int n_cap);
 int topk_max_row_entries();       // longest score row csa_topk supports
-cudaError_t launch_topk(const ha_params& p, const float* scores, int n_cap, const int32_t* q_pos,
+cudaError_t launch_topk(const ha_params& p, const void* scores, int n_cap, const int32_t* q_pos,
                         int Tq, int32_t* idx, void* ws, size_t ws_bytes, cudaStream_t st,
                         const StepOpts& so = StepOpts());
 

@@ -92,6 +92,17 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, i
       : "memory");
 }
 
+// 1-D bulk copy of `bytes` (a multiple of 16; both addresses 16-byte aligned)
+// global -> this CTA's shared memory, counted on `bar` (complete_tx).
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes,
+                                          uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+
 // ---------------------------------------------------------------- special functions
 // 2^x with the hardware approximation (relative error about 2^-22; results below
 // the smallest normal flush to zero, -inf gives +0).
@@ -187,6 +198,11 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool a_mn = 
          | (uint32_t(b_mn ? 1 : 0) << 16)   // B major-ness
          | (uint32_t(N >> 3) << 17)         // N / 8
          | (uint32_t(M >> 4) << 24);        // M / 16
+}
+
+// The same with f16 A and B (both operands must then be f16).
+__host__ __device__ constexpr uint32_t idesc_f16_f32(int M, int N) {
+  return idesc_bf16_f32(M, N) & ~((1u << 7) | (1u << 10));
 }
 
 // D[tmem] (+)= A[smem] * B[smem]^T, issued by one thread.

@@ -56,6 +56,13 @@ __device__ __forceinline__ T block_inclusive_scan(T v, T* scratch, T* total) {
   return res;
 }
 
+// A score as float: float32 scores, or bfloat16 scores (the FP4 indexer's), widened
+// exactly, so the same order-preserving keys serve both.
+__device__ __forceinline__ float score_at(const float* s, long long i) { return __ldg(s + i); }
+__device__ __forceinline__ float score_at(const __nv_bfloat16* s, long long i) {
+  return __uint_as_float(uint32_t(__ldg(reinterpret_cast<const unsigned short*>(s) + i)) << 16);
+}
+
 // ------------------------------------------------------------------ one CTA per row
 constexpr int kRowThreads = 1024;
 constexpr int kRowWarps = kRowThreads / 32;
@@ -140,7 +147,8 @@ __device__ __forceinline__ void row_radix(RowShared& sh, int count, int k, KeyAt
   need_eq = remaining;
 }
 
-__global__ void __launch_bounds__(kRowThreads) topk_row(const float* __restrict__ scores,
+template <typename S>
+__global__ void __launch_bounds__(kRowThreads) topk_row(const S* __restrict__ scores,
                                                        int n_cap, const int32_t* __restrict__ q_pos,
                                                        int pos_off, int k, int n_win, int m,
                                                        int elig, int32_t* __restrict__ idx) {
@@ -158,14 +166,14 @@ __global__ void __launch_bounds__(kRowThreads) topk_row(const float* __restrict_
   const int words = (n + 31) / 32;
   uint32_t* keys = skeys;                         // key i at pad32(i)
   uint32_t* region = skeys + words * 33;
-  const float* s = scores + (long long)row * n_cap;
+  const S* s = scores + (long long)row * n_cap;
   // keys in, sixteen loads in flight per thread
   for (int base = 0; base < n; base += 16 * kRowThreads) {
     float v[16];
 #pragma unroll
     for (int u = 0; u < 16; ++u) {
       const int i = base + u * kRowThreads + tid;
-      v[u] = i < n ? __ldg(s + i) : 0.f;
+      v[u] = i < n ? score_at(s, i) : 0.f;
     }
 #pragma unroll
     for (int u = 0; u < 16; ++u) {
@@ -302,7 +310,8 @@ struct SegMeta {
   uint32_t g;                            // the segment's threshold (0 for an empty segment)
 };
 
-__global__ void __launch_bounds__(kRowThreads) topk_seg(const float* __restrict__ scores,
+template <typename S>
+__global__ void __launch_bounds__(kRowThreads) topk_seg(const S* __restrict__ scores,
                                                        int n_cap, const int32_t* __restrict__ q_pos,
                                                        int pos_off, int k, int n_win, int m,
                                                        int elig, int C,
@@ -320,13 +329,13 @@ __global__ void __launch_bounds__(kRowThreads) topk_seg(const float* __restrict_
     return;
   }
   uint32_t* keys = skeys;                         // key i of the segment at pad32(i)
-  const float* s = scores + (long long)row * n_cap + lo;
+  const S* s = scores + (long long)row * n_cap + lo;
   for (int base = 0; base < len; base += 16 * kRowThreads) {
     float v[16];
 #pragma unroll
     for (int u = 0; u < 16; ++u) {
       const int i = base + u * kRowThreads + tid;
-      v[u] = i < len ? __ldg(s + i) : 0.f;
+      v[u] = i < len ? score_at(s, i) : 0.f;
     }
 #pragma unroll
     for (int u = 0; u < 16; ++u) {
@@ -372,8 +381,9 @@ __global__ void __launch_bounds__(kRowThreads) topk_seg(const float* __restrict_
   if (tid == 0) meta[blockIdx.x] = SegMeta{total, g};
 }
 
+template <typename S>
 __global__ void __launch_bounds__(kRowThreads) topk_seg_merge(
-    const float* __restrict__ scores, int n_cap, const int32_t* __restrict__ q_pos, int pos_off,
+    const S* __restrict__ scores, int n_cap, const int32_t* __restrict__ q_pos, int pos_off,
     int k, int n_win, int m, int elig, int C, const SegMeta* __restrict__ meta,
     const uint2* __restrict__ cand, int32_t* __restrict__ idx) {
   extern __shared__ uint32_t smem[];
@@ -467,15 +477,15 @@ __global__ void __launch_bounds__(kRowThreads) topk_seg_merge(
   }
   // fallback: digit passes over every score of the row (global memory), then an
   // ordered write over per-thread contiguous ranges
-  const float* s = scores + (long long)row * n_cap;
+  const S* s = scores + (long long)row * n_cap;
   uint32_t prefix, pmask;
   int need_eq;
-  row_radix(sh, n, k, [&](int i) { return score_key(__ldg(s + i)); }, prefix, pmask, need_eq);
+  row_radix(sh, n, k, [&](int i) { return score_key(score_at(s, i)); }, prefix, pmask, need_eq);
   const int kpt = (n + kRowThreads - 1) / kRowThreads;
   const int a = min(n, tid * kpt), b = min(n, a + kpt);
   int c_gt = 0, c_eq = 0;
   for (int i = a; i < b; ++i) {
-    const uint32_t km = score_key(__ldg(s + i)) & pmask;
+    const uint32_t km = score_key(score_at(s, i)) & pmask;
     c_gt += km > prefix ? 1 : 0;
     c_eq += km == prefix ? 1 : 0;
   }
@@ -483,7 +493,7 @@ __global__ void __launch_bounds__(kRowThreads) topk_seg_merge(
   int gt_before = block_inclusive_scan<kRowThreads, int>(c_gt, sh.scratch, &t_gt) - c_gt;
   int eq_before = block_inclusive_scan<kRowThreads, int>(c_eq, sh.scratch, &t_eq) - c_eq;
   for (int i = a; i < b; ++i) {
-    const uint32_t km = score_key(__ldg(s + i)) & pmask;
+    const uint32_t km = score_key(score_at(s, i)) & pmask;
     if (km > prefix) {
       out[gt_before + min(eq_before, need_eq)] = i;
       ++gt_before;
@@ -534,16 +544,19 @@ size_t topk_workspace_bytes(const ha_params& p, int Tq, int n_cap) {
   return size_t(rows) * sp.C * (sizeof(SegMeta) + size_t(kSegCap) * sizeof(uint2));
 }
 
-cudaError_t launch_topk(const ha_params& p, const float* scores, int n_cap, const int32_t* q_pos,
-                        int Tq, int32_t* idx, void* ws, size_t ws_bytes, cudaStream_t st,
-                        const StepOpts& so) {
+namespace {
+
+template <typename S>
+cudaError_t launch_topk_t(const ha_params& p, const S* scores, int n_cap, const int32_t* q_pos,
+                          int Tq, int32_t* idx, void* ws, size_t ws_bytes, cudaStream_t st,
+                          const StepOpts& so) {
   const long long rows = (long long)p.B * Tq;
   if (rows == 0) return cudaSuccess;
   if (n_cap <= kRowMaxKeys) {                     // the row fits one CTA's shared memory
     const size_t smem = row_smem_bytes(n_cap);
-    cudaError_t e = ensure_smem(reinterpret_cast<const void*>(topk_row), smem);
+    cudaError_t e = ensure_smem(reinterpret_cast<const void*>(topk_row<S>), smem);
     if (e != cudaSuccess) return e;
-    return launch_pdl(topk_row, dim3(unsigned(rows)), dim3(kRowThreads), smem, st, 1u, scores,
+    return launch_pdl(topk_row<S>, dim3(unsigned(rows)), dim3(kRowThreads), smem, st, 1u, scores,
                       n_cap, q_pos, so.pos_off, p.k, p.n_win, p.m, p.elig, idx);
   }
   if (n_cap <= kMaxSegRowKeys) {                  // segments, then one merge per row
@@ -553,20 +566,32 @@ cudaError_t launch_topk(const ha_params& p, const float* scores, int n_cap, cons
     uint2* cand = static_cast<uint2*>(ws);
     SegMeta* meta = reinterpret_cast<SegMeta*>(cand + size_t(rows) * sp.C * kSegCap);
     const size_t smem1 = size_t(sp.seg_len / 32) * 33 * sizeof(uint32_t);
-    cudaError_t e = ensure_smem(reinterpret_cast<const void*>(topk_seg), smem1);
+    cudaError_t e = ensure_smem(reinterpret_cast<const void*>(topk_seg<S>), smem1);
     if (e != cudaSuccess) return e;
-    e = launch_pdl(topk_seg, dim3(unsigned(rows * sp.C)), dim3(kRowThreads), smem1, st, 1u, scores,
-                   n_cap, q_pos, so.pos_off, p.k, p.n_win, p.m, p.elig, sp.C, sp.seg_len, meta,
-                   cand);
+    e = launch_pdl(topk_seg<S>, dim3(unsigned(rows * sp.C)), dim3(kRowThreads), smem1, st, 1u,
+                   scores, n_cap, q_pos, so.pos_off, p.k, p.n_win, p.m, p.elig, sp.C, sp.seg_len,
+                   meta, cand);
     if (e != cudaSuccess) return e;
     const size_t smem2 = (size_t(2) * kMergeCap + sp.C + 1) * sizeof(uint32_t);
-    e = ensure_smem(reinterpret_cast<const void*>(topk_seg_merge), smem2);
+    e = ensure_smem(reinterpret_cast<const void*>(topk_seg_merge<S>), smem2);
     if (e != cudaSuccess) return e;
-    return launch_pdl(topk_seg_merge, dim3(unsigned(rows)), dim3(kRowThreads), smem2, st, 1u,
+    return launch_pdl(topk_seg_merge<S>, dim3(unsigned(rows)), dim3(kRowThreads), smem2, st, 1u,
                       scores, n_cap, q_pos, so.pos_off, p.k, p.n_win, p.m, p.elig, sp.C,
                       static_cast<const SegMeta*>(meta), static_cast<const uint2*>(cand), idx);
   }
   return cudaErrorNotSupported;                  // rows longer than kMaxSegRowKeys
+}
+
+}  // namespace
+
+cudaError_t launch_topk(const ha_params& p, const void* scores, int n_cap, const int32_t* q_pos,
+                        int Tq, int32_t* idx, void* ws, size_t ws_bytes, cudaStream_t st,
+                        const StepOpts& so) {
+  if (p.fmt & HA_FMT_IDX4)                        // bfloat16 scores of the FP4 indexer
+    return launch_topk_t(p, static_cast<const __nv_bfloat16*>(scores), n_cap, q_pos, Tq, idx, ws,
+                         ws_bytes, st, so);
+  return launch_topk_t(p, static_cast<const float*>(scores), n_cap, q_pos, Tq, idx, ws, ws_bytes,
+                       st, so);
 }
 
 }  // namespace ha

@@ -25,7 +25,7 @@ from .synth import Workload
 def params_for(w: Workload, Tq_override: int | None = None) -> B.Params:
     return B.make_params(w.B, w.H, w.d, w.n_win, w.m, w.k if w.kind == "csa" else 1,
                          w.H_I if w.kind == "csa" else 1, w.d_I if w.kind == "csa" else 8,
-                         B.F32 if w.dtype == "f32" else B.BF16, B.ELIG_DISJOINT, 0.0)
+                         B.F32 if w.dtype == "f32" else B.BF16, B.ELIG_DISJOINT, 0.0, w.fmt)
 
 
 class HybridLayer:
@@ -41,9 +41,17 @@ class HybridLayer:
         dt = w.torch_dtype
         self.ck = torch.empty((w.B, self.n_cap, w.d), dtype=dt, device=device)
         self.cv = torch.empty((w.B, self.n_cap, w.d), dtype=dt, device=device)
-        self.cki = torch.empty((w.B, self.n_cap, w.d_I), dtype=dt, device=device) if self.csa else None
+        self.fp4 = bool(w.fmt & B.FMT_IDX4)
+        if not self.csa:
+            self.cki = None
+        elif self.fp4:                      # 80-byte FP4 rows of the indexer keys
+            self.cki = torch.empty((w.B, self.n_cap, B.IDX4_ROW_BYTES), dtype=torch.uint8,
+                                   device=device)
+        else:
+            self.cki = torch.empty((w.B, self.n_cap, w.d_I), dtype=dt, device=device)
         Tq = w.Tq
-        self.scores = torch.empty((w.B, Tq, self.n_cap), dtype=torch.float32, device=device) if self.csa else None
+        sdt = torch.bfloat16 if self.fp4 else torch.float32
+        self.scores = torch.empty((w.B, Tq, self.n_cap), dtype=sdt, device=device) if self.csa else None
         self.idx = torch.empty((w.B, Tq, w.k), dtype=torch.int32, device=device) if self.csa else None
         self.o = torch.empty((w.B, Tq, w.H, w.d), dtype=dt, device=device)
         self.lse = torch.empty((w.B, Tq, w.H), dtype=torch.float32, device=device)

@@ -45,6 +45,7 @@ class Workload:
     plant_frac: float = 0.0
     plant_sigma: float = 0.0
     seed: int = 0
+    fmt: int = 0         # storage-format bits of the layer (2: FP4 indexer, bfloat16 scores)
 
     @property
     def n_blocks(self) -> int:
@@ -81,6 +82,11 @@ WORKLOADS = {
     "hca_decode_1m": Workload("hca_decode_1m", "hca", 4, 1 << 20, 128, 512, 128, 128, 1024, 64,
                               128, "bf16"),
 }
+# the same CSA decodes with the indexer in FP4 and bfloat16 index scores
+WORKLOADS["csa_decode_64k_fp4"] = replace(WORKLOADS["csa_decode_64k"], name="csa_decode_64k_fp4",
+                                          fmt=2)
+WORKLOADS["csa_decode_1m_fp4"] = replace(WORKLOADS["csa_decode_1m"], name="csa_decode_1m_fp4",
+                                         fmt=2)
 
 _TENSOR_IDS = {"k_tok": 1, "v_tok": 2, "ki_tok": 3, "gate": 4, "q": 5, "qI": 6, "w": 7,
                "plant": 8, "extra": 9}

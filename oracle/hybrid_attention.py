@@ -59,7 +59,7 @@ import numpy as np
 
 __all__ = [
     "round_to_bf16", "round_to_storage", "round_to_e4m3", "fp8_kv_encode", "fp8_kv_decode",
-    "round_to_e2m1", "fp4_encode", "fp4_decode",
+    "round_to_e2m1", "fp4_encode", "fp4_decode", "fp4_pack", "fp4_unpack",
     "gate_softmax", "compress_block",
     "compress", "n_eligible", "window_positions", "index_scores", "topk_select",
     "attend", "merge_partials", "csa_decode", "hca_decode", "prefill_query",
@@ -152,6 +152,11 @@ def fp8_kv_decode(rope, codes, scale):
 # e2m1 value (sign, 2 exponent bits, 1 mantissa bit: magnitudes 0, 0.5, 1, 1.5, 2,
 # 3, 4, 6) with one e4m3 scale per group, scale = max|x| / 6 rounded to e4m3,
 # codes rounded to nearest, ties to even, magnitudes above 6 saturating to 6.
+# The quantization decisions (amax / 6 and x / scale) are taken in float32, the
+# precision the kernels take them in, on the float32 values of the inputs, so
+# that both sides decide alike on the same inputs; the rounding steps themselves
+# are exact.  A row is stored as 80 bytes: 64 bytes of codes (element 2i in the
+# low nibble), the 8 scales, 8 unused bytes (fp4_pack / fp4_unpack).
 # --------------------------------------------------------------------------
 E2M1_MAX = 6.0
 FP4_GROUP = 16
@@ -174,14 +179,71 @@ def round_to_e2m1(x):
 
 def fp4_encode(rows):
     """Rows [n, d] (d a multiple of 16) -> (codes [n, d/16, 16] e2m1 values,
-    scales [n, d/16] e4m3 values); an all-zero group gets scale 0 and codes 0."""
+    scales [n, d/16] e4m3 values); an all-zero group gets scale 0 and codes 0.
+    The divisions are float32 divisions of the rows' float32 values."""
     rows = np.asarray(rows, dtype=np.float64)
     n, d = rows.shape
-    g = rows.reshape(n, d // FP4_GROUP, FP4_GROUP)
-    scale = round_to_e4m3(np.abs(g).max(axis=-1) / E2M1_MAX)
-    safe = np.where(scale > 0, scale, 1.0)
-    codes = np.where(scale[..., None] > 0, round_to_e2m1(g / safe[..., None]), 0.0)
+    g = rows.reshape(n, d // FP4_GROUP, FP4_GROUP).astype(np.float32)
+    amax = np.abs(g).max(axis=-1)
+    scale = round_to_e4m3((amax / np.float32(E2M1_MAX)).astype(np.float32))
+    safe = np.where(scale > 0, scale, 1.0).astype(np.float32)
+    quot = (g / safe[..., None]).astype(np.float32)
+    codes = np.where(scale[..., None] > 0, round_to_e2m1(quot), 0.0)
     return codes, scale
+
+
+def fp4_pack(codes, scale):
+    """The 80-byte rows of the FP4 indexer format: [n, 80] uint8."""
+    codes = np.asarray(codes, dtype=np.float64)
+    scale = np.asarray(scale, dtype=np.float64)
+    n = codes.shape[0]
+    flat = codes.reshape(n, -1)
+    mag = np.abs(flat)
+    grid = np.array([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0])
+    idx = np.searchsorted(grid, mag)
+    if not np.array_equal(grid[idx], mag):
+        raise ValueError("codes off the e2m1 grid")
+    nib = (idx | np.where(np.signbit(flat), 8, 0)).astype(np.uint8)
+    out = np.zeros((n, 80), dtype=np.uint8)
+    out[:, :64] = nib[:, 0::2] | (nib[:, 1::2] << 4)
+    out[:, 64:72] = _e4m3_bits(scale)
+    return out
+
+
+def fp4_unpack(rows):
+    """Inverse of fp4_pack: (codes [n, 8, 16], scales [n, 8]) as float64 values."""
+    rows = np.asarray(rows, dtype=np.uint8)
+    n = rows.shape[0]
+    grid = np.array([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0])
+    nib = np.empty((n, 128), dtype=np.uint8)
+    nib[:, 0::2] = rows[:, :64] & 15
+    nib[:, 1::2] = rows[:, :64] >> 4
+    codes = np.where(nib & 8, -1.0, 1.0) * grid[nib & 7]
+    return codes.reshape(n, 8, 16), _e4m3_value(rows[:, 64:72])
+
+
+def _e4m3_bits(v):
+    """e4m3fn bit patterns of values on the e4m3fn grid (finite, sign of zero kept)."""
+    v = np.asarray(v, dtype=np.float64)
+    a = np.abs(v)
+    bits = np.zeros(v.shape, dtype=np.int64)
+    nz = a > 0
+    e = np.floor(np.log2(np.where(nz, a, 1.0))).astype(np.int64)
+    sub = nz & (e < -6)
+    norm = nz & ~sub
+    bits = np.where(norm, ((e + 7) << 3) | np.rint((a / np.exp2(e) - 1.0) * 8).astype(np.int64), bits)
+    bits = np.where(sub, np.rint(a / 2.0 ** -9).astype(np.int64), bits)
+    if not np.array_equal(_e4m3_value(bits.astype(np.uint8)), a):
+        raise ValueError("values off the e4m3 grid")
+    return (bits | np.where(np.signbit(v), 128, 0)).astype(np.uint8)
+
+
+def _e4m3_value(bits):
+    """Values of e4m3fn bit patterns (no NaN pattern expected)."""
+    b = np.asarray(bits, dtype=np.int64)
+    e, mnt = (b >> 3) & 15, b & 7
+    val = np.where(e == 0, mnt * 2.0 ** -9, (1.0 + mnt / 8.0) * np.exp2(e - 7.0))
+    return np.where(b & 128, -val, val)
 
 
 def fp4_decode(codes, scale):

@@ -36,7 +36,7 @@ def test_every_header_symbol_is_exported(lib):
 
 
 def test_version_and_status_strings(lib):
-    assert B.ha_abi_version() == 2
+    assert B.ha_abi_version() == 3
     for code in range(6):
         assert B.ha_status_string(code) not in ("", "unknown status")
     assert B.ha_status_string(99) == "unknown status"

@@ -16,6 +16,7 @@ scores, and from scores of FP4 queries and keys, against the exact top-k.
 import math
 
 import numpy as np
+import torch
 import pytest
 
 import oracle as O
@@ -139,3 +140,40 @@ def test_recall_of_the_indexer_formats_with_a_planted_subset():
     r_bf16, r_fp4 = len(exact & bf16) / k, len(exact & fp4) / k
     print(f"recall with a planted subset: bf16 scores {r_bf16:.4f}, fp4 indexer {r_fp4:.4f}")
     assert r_bf16 >= 0.97 and r_fp4 >= 0.85
+
+
+def test_fp4_row_bytes_worked_example_and_round_trip():
+    """The 80-byte row: element 2i in the low nibble (sign in bit 3, magnitude index
+    into 0, .5, 1, 1.5, 2, 3, 4, 6), the 8 e4m3fn scales after the 64 code bytes."""
+    codes = np.zeros((1, 8, 16))
+    scale = np.zeros((1, 8))
+    codes[0, 0, 0], codes[0, 0, 1] = 1.0, -6.0        # nibbles 2 and 8|7 -> byte 0xF2
+    codes[0, 7, 15] = 0.5                             # element 127 -> high nibble of byte 63
+    scale[0] = [1.0, 448.0, 2.0 ** -9, -2.0, 0.0, 0.75, 1.125, 240.0]
+    row = O.fp4_pack(codes, scale)
+    assert row.shape == (1, 80) and row.dtype == np.uint8
+    assert row[0, 0] == 0xF2 and row[0, 63] == 0x10 and (row[0, 1:63] == 0).all()
+    assert row[0, 64:72].tolist() == [0x38, 0x7E, 0x01, 0xC0, 0x00, 0x34, 0x39, 0x77]
+    assert (row[0, 72:] == 0).all()
+    c2, s2 = O.fp4_unpack(row)
+    assert np.array_equal(c2, codes) and np.array_equal(s2, scale)
+
+
+def test_fp4_scale_bits_match_torch_float8():
+    """The scale bytes are torch's float8_e4m3fn bit patterns of the same values."""
+    rng = np.random.default_rng(9)
+    v = O.round_to_e4m3(rng.standard_normal(4000) * np.exp2(rng.uniform(-8, 8, 4000)))
+    v = v[np.isfinite(v)]
+    ref = torch.from_numpy(v).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    codes = np.zeros((len(v), 8, 16))
+    scale = np.zeros((len(v), 8))
+    scale[:, 0] = v
+    assert np.array_equal(O.fp4_pack(codes, scale)[:, 64], ref)
+
+
+def test_fp4_pack_round_trips_encoded_rows():
+    rng = np.random.default_rng(10)
+    rows = rng.standard_normal((64, 128)) / math.sqrt(128)
+    codes, scale = O.fp4_encode(rows)
+    c2, s2 = O.fp4_unpack(O.fp4_pack(codes, scale))
+    assert np.array_equal(O.fp4_decode(c2, s2), O.fp4_decode(codes, scale))
