@@ -173,8 +173,10 @@ def workload_config(w, l2: str, timing: str) -> dict:
     cfg.update({"H": w.H, "d": w.d, "n_win": w.n_win, "m": w.m, "k": w.k if csa else None,
                 "H_I": w.H_I if csa else None, "d_I": w.d_I if csa else None,
                 "l2": l2, "timing": timing})
-    if w.fmt:
+    if w.fmt & 2:
         cfg["indexer_format"] = "FP4 keys and queries (e2m1, e4m3 scale per 16), bfloat16 scores"
+    if w.fmt & 1:
+        cfg["kv_format"] = "compressed K/V: RoPE dims bfloat16, other dims e4m3 + float32 scale per 64"
     return cfg
 
 
@@ -209,20 +211,22 @@ def profiled_traffic(workload: str | None, kernel_name: str, source_file: str):
 
 def step_bytes(w, n_elig: int, n_keys_win: int):
     es = 2 if w.dtype == "bf16" else 4
+    row_b = 608 if w.fmt & 1 else w.d * es      # a compressed K or V row
     out = {}
     if w.kind == "csa":
         # FP4 indexer: 80-byte key rows, bfloat16 scores
         key_b = 80 if w.fmt & 2 else w.d_I * es
         score_b = 2 if w.fmt & 2 else 4
-        out["compress"] = w.B * (w.m * (2 * w.d + w.d_I) * es + w.m * 4 + 2 * w.d * es + key_b)
+        out["compress"] = w.B * (w.m * (2 * w.d + w.d_I) * es + w.m * 4 + 2 * row_b + key_b)
         out["index"] = w.B * (n_elig * key_b + n_elig * score_b + w.H_I * w.d_I * es + w.H_I * 4)
         out["topk"] = w.B * (n_elig * score_b + w.k * 4)
-        keys = min(w.k, n_elig) + n_keys_win
-        out["attention"] = w.B * (keys * 2 * w.d * es + 2 * w.H * w.d * es + w.k * 4)
+        # FP8 K/V: the selected entries' 608-byte rows (widened in L2), window bf16
+        out["attention"] = w.B * (min(w.k, n_elig) * 2 * row_b + n_keys_win * 2 * w.d * es
+                                  + 2 * w.H * w.d * es + w.k * 4)
     else:
-        out["compress"] = w.B * (w.m * 2 * w.d * es + w.m * 4 + 2 * w.d * es)
-        keys = n_elig + n_keys_win
-        out["attention"] = w.B * (keys * 2 * w.d * es + 2 * w.H * w.d * es)
+        out["compress"] = w.B * (w.m * 2 * w.d * es + w.m * 4 + 2 * row_b)
+        out["attention"] = w.B * (n_elig * 2 * row_b + n_keys_win * 2 * w.d * es
+                                  + 2 * w.H * w.d * es)
     return out
 
 
@@ -235,7 +239,8 @@ def bulk_compress_rate(w, layer, dev, reps: int = 3) -> dict:
     n_blk = layer.n_cap
     es = 2 if w.dtype == "bf16" else 4
     rows = (2 * w.d + (w.d_I if w.kind == "csa" else 0)) * es
-    rows_out = 2 * w.d * es + ((80 if w.fmt & 2 else w.d_I * es) if w.kind == "csa" else 0)
+    rows_out = 2 * (608 if w.fmt & 1 else w.d * es) + \
+        ((80 if w.fmt & 2 else w.d_I * es) if w.kind == "csa" else 0)
     nbytes = w.B * n_blk * (w.m * (rows + 4) + rows_out)
     flush_w = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)

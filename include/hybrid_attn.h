@@ -79,6 +79,15 @@ typedef enum { HA_F32 = 0, HA_BF16 = 1 } ha_dtype;
 
 /* Storage formats of the deployed model ([V4-notes] §8), bit flags of
  * ha_params.fmt; both need dtype HA_BF16.
+ *   HA_FMT_KV8: the compressed K/V caches keep their RoPE dims in BF16 and the
+ *     other dims in FP8.  With d = 512 a row of ck or cv is 608 bytes: dims
+ *     0..63 as bfloat16, dims 64..511 as e4m3fn codes, one float32 scale per 64
+ *     dims (7), 4 unused bytes; element value = code * scale, scale = amax / 448
+ *     of its group, code = e4m3(x / scale) nearest even, the divisions in
+ *     float32 (an all-zero group has scale 0 and codes 0).  ck and cv are then
+ *     [B, n_cap, 608] bytes; the per-token caches stay bfloat16.  The attention
+ *     calls widen the rows they read to bfloat16 (code * scale rounded to nearest
+ *     even) in their workspace first.  Needs d = 512.
  *   HA_FMT_IDX4: the Lightning Indexer computes in FP4 and keeps its scores in
  *     BF16.  Compressed indexer keys (cki) are rows of 80 bytes: d_I = 128
  *     e2m1 codes, two per byte (element 2i in the low nibble), then 8 e4m3fn
@@ -90,7 +99,7 @@ typedef enum { HA_F32 = 0, HA_BF16 = 1 } ha_dtype;
  *     same way inside the indexer.  Index scores are bfloat16 (the float32 sum
  *     rounded to nearest even): csa_index_scores writes them and csa_topk reads
  *     them.  Needs H_I = 64 and d_I = 128. */
-enum { HA_FMT_IDX4 = 2 };
+enum { HA_FMT_KV8 = 1, HA_FMT_IDX4 = 2 };
 typedef enum { HA_ELIG_DISJOINT = 0, HA_ELIG_OVERLAP = 1 } ha_elig;
 typedef enum { HA_OP_TOPK = 0, HA_OP_DECODE = 1, HA_OP_PREFILL = 2, HA_OP_DECODE_STEP = 3 } ha_op;
 

@@ -35,7 +35,9 @@ class Params(ctypes.Structure):
                 ("elig", ctypes.c_int32), ("scale", ctypes.c_float), ("fmt", ctypes.c_int32)]
 
 
+FMT_KV8 = 1            # compressed K/V rows: RoPE dims bf16, the rest e4m3 (608 bytes)
 FMT_IDX4 = 2           # FP4 indexer keys and queries, bfloat16 index scores
+KV8_ROW_BYTES = 608    # one FP8 K or V row (d = 512)
 IDX4_ROW_BYTES = 80    # one FP4 indexer key row (d_I = 128)
 
 

@@ -130,7 +130,9 @@ ha_status check_params(const ha_params* p, bool need_attn, bool need_index) {
     HA_REQUIRE(p->H >= 1 && p->H <= 256, HA_ERR_UNSUPPORTED, "H = %d (1..256)", p->H);
     HA_REQUIRE(isfinite(p->scale), HA_ERR_INVALID_ARG, "scale is not finite");
   }
-  HA_REQUIRE((p->fmt & ~HA_FMT_IDX4) == 0, HA_ERR_INVALID_ARG, "fmt = %d", p->fmt);
+  HA_REQUIRE((p->fmt & ~(HA_FMT_IDX4 | HA_FMT_KV8)) == 0, HA_ERR_INVALID_ARG, "fmt = %d", p->fmt);
+  HA_REQUIRE(!(p->fmt & HA_FMT_KV8) || p->d == 512, HA_ERR_UNSUPPORTED,
+             "the FP8 KV format needs d = 512 (d = %d)", p->d);
   HA_REQUIRE(p->fmt == 0 || p->dtype == HA_BF16, HA_ERR_UNSUPPORTED,
              "storage formats need bfloat16 (fmt = %d)", p->fmt);
   if ((p->fmt & HA_FMT_IDX4) && need_index)
@@ -196,11 +198,36 @@ namespace {
 
 size_t round_up256(size_t x) { return (x + 255) / 256 * 256; }
 
+// Workspace of an attention call: the plan's split partials, then, for FP8 K/V
+// rows, the rows widened to bfloat16 (the selected entries of a decode selection,
+// else every entry of the cache).
+size_t attn_ws_bytes(const ha_params* p, const ha::AttnPlan& pl, int n_cap, bool select) {
+  if (!(p->fmt & HA_FMT_KV8)) return pl.ws_bytes;
+  return round_up256(pl.ws_bytes) + ha::kv8_expand_bytes(*p, n_cap, select);
+}
+
+// FP8 K/V rows: widen the rows the attention reads into the workspace (after the
+// partials) and point ck, cv, n_cap and (selection) idx at the widened view.
+cudaError_t kv8_view(const ha_params* p, const ha::AttnPlan& pl, const void*& ck, const void*& cv,
+                     int& n_cap, const int32_t*& idx, bool select, const int32_t* ctx_len,
+                     void* ws, cudaStream_t st) {
+  if (!(p->fmt & HA_FMT_KV8)) return cudaSuccess;
+  ha::KvExpanded ex{};
+  cudaError_t e = ha::launch_kv8_expand(*p, ck, cv, n_cap, select ? idx : nullptr, ctx_len,
+                                        static_cast<char*>(ws) + round_up256(pl.ws_bytes), &ex, st);
+  if (e != cudaSuccess) return e;
+  ck = ex.ck;
+  cv = ex.cv;
+  n_cap = ex.n_cap;
+  if (select) idx = ex.idx;
+  return cudaSuccess;
+}
+
 // Workspace of a fused decode step: the top-k part (segmented rows), then the
-// attention partials.
+// attention's.
 size_t step_workspace_bytes(const ha_params* p, int n_cap, int tok_cap, bool is_csa) {
   const size_t topk = is_csa ? round_up256(ha::topk_workspace_bytes(*p, 1, n_cap)) : 0;
-  return topk + attention_plan(p, p->B, n_cap, tok_cap, is_csa, true).ws_bytes;
+  return topk + attn_ws_bytes(p, attention_plan(p, p->B, n_cap, tok_cap, is_csa, true), n_cap, is_csa);
 }
 
 // Checks shared by the two fused decode steps (everything but the indexer inputs).
@@ -225,7 +252,7 @@ ha_status check_step(const ha_params* p, const void* q, const void* k_tok, const
 }  // namespace
 
 size_t ha::decode_workspace_bytes(const ha_params* p, int n_cap, int tok_cap, bool is_csa) {
-  return attention_plan(p, p->B, n_cap, tok_cap, is_csa, true).ws_bytes;
+  return attn_ws_bytes(p, attention_plan(p, p->B, n_cap, tok_cap, is_csa, true), n_cap, is_csa);
 }
 
 void ha::set_last_error(const char* msg) {
@@ -366,8 +393,12 @@ ha_status hybrid_attn_decode(const ha_params* p, const void* q, const void* ck, 
   HA_REQUIRE(n_cap >= 1, HA_ERR_INVALID_ARG, "n_cap = %d", n_cap);
   const bool tc = ha::attention_tc_supported(*p, n_cap, tok_cap);
   const ha::AttnPlan pl = attention_plan(p, p->B, n_cap, tok_cap, idx != nullptr, true);
-  HA_REQUIRE(ws_bytes >= pl.ws_bytes && (pl.ws_bytes == 0 || ws != nullptr), HA_ERR_WORKSPACE,
-             "workspace %zu bytes < %zu", ws_bytes, pl.ws_bytes);
+  const size_t need = attn_ws_bytes(p, pl, n_cap, idx != nullptr);
+  HA_REQUIRE(ws_bytes >= need && (need == 0 || ws != nullptr), HA_ERR_WORKSPACE,
+             "workspace %zu bytes < %zu", ws_bytes, need);
+  cudaError_t e = kv8_view(p, pl, ck, cv, n_cap, idx, idx != nullptr, ctx_len, ws,
+                           (cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_status(e, "decode: FP8 K/V widening launch");
   if (tc) {
     int* err = ha::device_error_word();
     HA_REQUIRE(err != nullptr, HA_ERR_CUDA, "device error word unavailable");
@@ -428,8 +459,12 @@ ha_status hybrid_attn_prefill(const ha_params* p, const void* q, const int32_t* 
              p->n_win);
   const bool tc = ha::attention_tc_supported(*p, n_cap, tok_cap);
   const ha::AttnPlan pl = attention_plan(p, p->B * Tq, n_cap, tok_cap, idx != nullptr, false);
-  HA_REQUIRE(ws_bytes >= pl.ws_bytes && (pl.ws_bytes == 0 || ws != nullptr), HA_ERR_WORKSPACE,
-             "workspace %zu bytes < %zu", ws_bytes, pl.ws_bytes);
+  const size_t need = attn_ws_bytes(p, pl, n_cap, false);
+  HA_REQUIRE(ws_bytes >= need && (need == 0 || ws != nullptr), HA_ERR_WORKSPACE,
+             "workspace %zu bytes < %zu", ws_bytes, need);
+  // FP8 K/V: every entry widened (each query has its own selection)
+  cudaError_t e = kv8_view(p, pl, ck, cv, n_cap, idx, false, q_pos, ws, (cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_status(e, "prefill: FP8 K/V widening launch");
   if (tc) {
     int* err = ha::device_error_word();
     HA_REQUIRE(err != nullptr, HA_ERR_CUDA, "device error word unavailable");
@@ -468,7 +503,7 @@ ha_status csa_decode_step(const ha_params* p, const void* q, const void* q_idx,
              ha::topk_max_row_entries());
   const size_t topk_ws = round_up256(ha::topk_workspace_bytes(*p, 1, n_cap));
   const ha::AttnPlan pl = attention_plan(p, p->B, n_cap, tok_cap, true, true);
-  const size_t need = topk_ws + pl.ws_bytes;
+  const size_t need = topk_ws + attn_ws_bytes(p, pl, n_cap, true);
   HA_REQUIRE(ws_bytes >= need && (need == 0 || ws != nullptr), HA_ERR_WORKSPACE,
              "workspace %zu bytes < %zu", ws_bytes, need);
   int* err = ha::device_error_word();
@@ -500,15 +535,21 @@ ha_status csa_decode_step(const ha_params* p, const void* q, const void* q_idx,
   sk.pos_off = -1;
   e = ha::launch_topk(*p, scores, n_cap, ctx_len, 1, idx, ws, topk_ws, st, sk);
   if (e != cudaSuccess) return cuda_status(e, "step: top-k launch");
-  void* attn_ws = pl.ws_bytes ? static_cast<char*>(ws) + topk_ws : nullptr;
+  void* attn_ws = need > topk_ws ? static_cast<char*>(ws) + topk_ws : nullptr;
+  const void* ck_a = ck;
+  const void* cv_a = cv;
+  int n_cap_a = n_cap;
+  const int32_t* idx_a = idx;
+  e = kv8_view(p, pl, ck_a, cv_a, n_cap_a, idx_a, true, ctx_len, attn_ws, st);
+  if (e != cudaSuccess) return cuda_status(e, "step: FP8 K/V widening launch");
   if (ha::attention_tc_supported(*p, n_cap, tok_cap)) {
     ha::StepOpts sa;
     sa.early = 1;
-    e = ha::launch_attention_tc(*p, pl, 1, 1, q, ctx_len, ck, cv, n_cap, idx, k_tok, v_tok,
+    e = ha::launch_attention_tc(*p, pl, 1, 1, q, ctx_len, ck_a, cv_a, n_cap_a, idx_a, k_tok, v_tok,
                                 tok_cap, o, lse, attn_ws, err, st, sa);
   } else {
-    e = ha::launch_attention_simt(*p, pl, 1, 1, q, ctx_len, ck, cv, n_cap, idx, k_tok, v_tok,
-                                  tok_cap, o, lse, attn_ws, st);
+    e = ha::launch_attention_simt(*p, pl, 1, 1, q, ctx_len, ck_a, cv_a, n_cap_a, idx_a, k_tok,
+                                  v_tok, tok_cap, o, lse, attn_ws, st);
   }
   return cuda_status(e, "step: attention launch");
 }
@@ -525,8 +566,9 @@ ha_status hca_decode_step(const ha_params* p, const void* q, const void* k_tok, 
   if (s != HA_OK) return s;
   HA_OPT_PTR(ws);
   const ha::AttnPlan pl = attention_plan(p, p->B, n_cap, tok_cap, false, true);
-  HA_REQUIRE(ws_bytes >= pl.ws_bytes && (pl.ws_bytes == 0 || ws != nullptr), HA_ERR_WORKSPACE,
-             "workspace %zu bytes < %zu", ws_bytes, pl.ws_bytes);
+  const size_t need = attn_ws_bytes(p, pl, n_cap, false);
+  HA_REQUIRE(ws_bytes >= need && (need == 0 || ws != nullptr), HA_ERR_WORKSPACE,
+             "workspace %zu bytes < %zu", ws_bytes, need);
   const cudaStream_t st = (cudaStream_t)stream;
   // As in csa_decode_step: under the disjoint rule with n_win >= m the attention
   // reads no entry the compressor writes, so it runs beside the compression and
@@ -540,16 +582,24 @@ ha_status hca_decode_step(const ha_params* p, const void* q, const void* k_tok, 
   const int dims[2] = {p->d, p->d};
   cudaError_t e = ha::launch_compress(*p, 2, src, dst, dims, gate, nullptr, 1, tok_cap, n_cap, st, sc);
   if (e != cudaSuccess) return cuda_status(e, "step: compress launch");
+  // FP8 K/V: the widening (which waits for the compressor) comes first, and the
+  // attention, reading the widened rows, then waits for it as usual
+  const void* ck_a = ck;
+  const void* cv_a = cv;
+  int n_cap_a = n_cap;
+  const int32_t* no_idx = nullptr;
+  e = kv8_view(p, pl, ck_a, cv_a, n_cap_a, no_idx, false, ctx_len, ws, st);
+  if (e != cudaSuccess) return cuda_status(e, "step: FP8 K/V widening launch");
   if (ha::attention_tc_supported(*p, n_cap, tok_cap)) {
     int* err = ha::device_error_word();
     HA_REQUIRE(err != nullptr, HA_ERR_CUDA, "device error word unavailable");
     ha::StepOpts sa;
-    sa.wait_last = overlap ? 1 : 0;
-    e = ha::launch_attention_tc(*p, pl, 1, 1, q, ctx_len, ck, cv, n_cap, nullptr, k_tok, v_tok,
-                                tok_cap, o, lse, ws, err, st, sa);
+    sa.wait_last = overlap && !(p->fmt & HA_FMT_KV8) ? 1 : 0;
+    e = ha::launch_attention_tc(*p, pl, 1, 1, q, ctx_len, ck_a, cv_a, n_cap_a, nullptr, k_tok,
+                                v_tok, tok_cap, o, lse, ws, err, st, sa);
   } else {
-    e = ha::launch_attention_simt(*p, pl, 1, 1, q, ctx_len, ck, cv, n_cap, nullptr, k_tok, v_tok,
-                                  tok_cap, o, lse, ws, st);
+    e = ha::launch_attention_simt(*p, pl, 1, 1, q, ctx_len, ck_a, cv_a, n_cap_a, nullptr, k_tok,
+                                  v_tok, tok_cap, o, lse, ws, st);
   }
   return cuda_status(e, "step: attention launch");
 }
@@ -565,10 +615,12 @@ ha_status ha_workspace_size(const ha_params* p, int32_t op, int32_t Tq, int32_t 
   switch (op) {
     case HA_OP_TOPK: *bytes = ha::topk_workspace_bytes(*p, Tq, n_cap); return HA_OK;
     case HA_OP_DECODE:
-      *bytes = attention_plan(p, p->B, n_cap, 0, is_csa != 0, true).ws_bytes;
+      *bytes = attn_ws_bytes(p, attention_plan(p, p->B, n_cap, 0, is_csa != 0, true), n_cap,
+                             is_csa != 0);
       return HA_OK;
     case HA_OP_PREFILL:
-      *bytes = attention_plan(p, p->B * Tq, n_cap, 0, is_csa != 0, false).ws_bytes;
+      *bytes = attn_ws_bytes(p, attention_plan(p, p->B * Tq, n_cap, 0, is_csa != 0, false), n_cap,
+                             false);
       return HA_OK;
     case HA_OP_DECODE_STEP:
       *bytes = step_workspace_bytes(p, n_cap, 0, is_csa != 0);

@@ -34,7 +34,46 @@ struct CompressArgs {
   const int32_t* ctx_len;   // non-null: the block the newest token completes (n_blk = 1)
   int B, n_blk, m, tok_cap, n_cap;
   int fp4_third;            // the third tensor (indexer keys) is written in the FP4 format
+  int kv8;                  // K and V are written in the FP8 KV format (608-byte rows)
 };
+
+// Chunk `chunk` (8 dims, of 64 per row of d = 512) of a compressed K or V row in the
+// FP8 KV format: dims 0..63 as bfloat16 at byte 16 chunk; dims 64..511 as e4m3fn
+// codes at byte 128 + 8 (chunk - 8) with the float32 scale of their 64-dim group,
+// scale = amax / 448 (float32 division), at byte 576 + 4 group.  The 8 chunks of a
+// group sit on 8 consecutive lanes (lane % 8 == chunk % 8), all of which call this,
+// live or not, so that the group's amax can be reduced among them.
+__device__ __forceinline__ void write_kv8(unsigned char* row, int chunk, const float (&acc)[8],
+                                          bool live) {
+  const unsigned lane = threadIdx.x & 31;
+  const unsigned grp = 0xffu << (lane & 24u);
+  float amax = 0.f;
+  if (live && chunk >= 8)
+#pragma unroll
+    for (int e = 0; e < 8; ++e) amax = fmaxf(amax, fabsf(acc[e]));
+  amax = fmaxf(amax, __shfl_xor_sync(grp, amax, 1));
+  amax = fmaxf(amax, __shfl_xor_sync(grp, amax, 2));
+  amax = fmaxf(amax, __shfl_xor_sync(grp, amax, 4));
+  if (!live) return;
+  if (chunk < 8) {
+    st16(reinterpret_cast<__nv_bfloat16*>(row) + 8 * chunk, pack(acc));
+    return;
+  }
+  const float scale = __fdiv_rn(amax, 448.f);
+  uint32_t w[2] = {0u, 0u};
+  if (scale > 0.f) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      uint16_t r;
+      asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;"
+          : "=h"(r)
+          : "f"(__fdiv_rn(acc[2 * i + 1], scale)), "f"(__fdiv_rn(acc[2 * i], scale)));
+      w[i >> 1] |= uint32_t(r) << (16 * (i & 1));
+    }
+  }
+  *reinterpret_cast<uint2*>(row + 128 + 8 * (chunk - 8)) = make_uint2(w[0], w[1]);
+  if ((chunk & 7) == 0) *reinterpret_cast<float*>(row + 576 + 4 * ((chunk - 8) >> 3)) = scale;
+}
 
 // First block to compress for sequence b: blk_begin[b], or the block completed by
 // the newest token (ctx_len[b] / m - 1 when ctx_len[b] is a positive multiple of m,
@@ -80,9 +119,9 @@ struct SmallItem {
   uint4 raw[MM];
   float g[MM];
   T* dst;
-  unsigned char* row4;   // FP4 indexer-key row (fp4_third), else null
-  int chunk;
-  bool live;
+  unsigned char* row4;   // FP4 indexer-key row (fp4_third) or FP8 K / V row (kv8), else null
+  int chunk, tensor;
+  bool live, in_range;
 };
 
 template <typename T, int M>     // M > 0: block size fixed at compile time
@@ -103,8 +142,14 @@ __global__ void __launch_bounds__(256) compress_small_m(CompressArgs a) {
       const long long it = base + k * stride;
       itm[k].live = false;
       itm[k].row4 = nullptr;
+      itm[k].in_range = it < n_items;
       if (it >= n_items) continue;
       const int c = int(it % total_chunks);
+      {
+        const ChunkRef r0 = chunk_ref(a, c);
+        itm[k].tensor = r0.tensor;
+        itm[k].chunk = r0.chunk;
+      }
       const long long task = it / total_chunks;
       const int b = int(task / a.n_blk);
       const int fb = first_block(a, b);
@@ -127,7 +172,8 @@ __global__ void __launch_bounds__(256) compress_small_m(CompressArgs a) {
       if (a.fp4_third && r.tensor == 2)
         itm[k].row4 = static_cast<unsigned char*>(a.dst[2]) +
                       ((long long)b * a.n_cap + j) * fp4::kRowBytes;
-      itm[k].chunk = r.chunk;
+      if (a.kv8 && r.tensor < 2)
+        itm[k].row4 = static_cast<unsigned char*>(r.dst) + ((long long)b * a.n_cap + j) * 608;
       itm[k].live = true;
     }
 #pragma unroll
@@ -157,6 +203,10 @@ __global__ void __launch_bounds__(256) compress_small_m(CompressArgs a) {
       }
       }
       if constexpr (V == 8) {
+        if (a.kv8 && itm[k].in_range && itm[k].tensor < 2) {
+          write_kv8(itm[k].row4, itm[k].chunk, acc, itm[k].live);
+          continue;
+        }
         if (a.fp4_third) {
           // FP4 indexer keys: a 16-element group is the chunk pair (2g, 2g + 1), held
           // by lanes (2l, 2l + 1) (items and chunks alternate parity alike, and both
@@ -287,6 +337,13 @@ __global__ void __launch_bounds__(kMaxGroups * kSlice) compress_large_m(Compress
 #pragma unroll
       for (int e = 0; e < V; ++e) acc[e] += part[(g2 * kSlice + lane_c) * V + e];
     }
+    if constexpr (V == 8) {
+      if (a.kv8 && r.tensor < 2) {   // a slice of 32 chunks holds whole 8-chunk groups
+        write_kv8(static_cast<unsigned char*>(r.dst) + ((long long)b * a.n_cap + j) * 608,
+                  r.chunk, acc, true);
+        return;
+      }
+    }
     T* dst = static_cast<T*>(r.dst) + ((long long)b * a.n_cap + j) * rowb;
     st16(dst + r.chunk * V, pack(acc));
   }
@@ -320,6 +377,7 @@ cudaError_t launch_compress(const ha_params& p, int n_tensors, const void* const
   CompressArgs a{};
   a.ctx_len = so.ctx_len;
   a.fp4_third = (p.fmt & HA_FMT_IDX4) && n_tensors == 3 ? 1 : 0;
+  a.kv8 = (p.fmt & HA_FMT_KV8) ? 1 : 0;
   const int V = p.dtype == HA_BF16 ? 8 : 4;
   for (int i = 0; i < 3; ++i) {
     a.src[i] = i < n_tensors ? src[i] : nullptr;

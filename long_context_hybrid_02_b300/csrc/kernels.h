@@ -77,6 +77,21 @@ cudaError_t launch_attention_simt(const ha_params& p, const AttnPlan& pl, int de
 cudaError_t launch_attn_merge(const ha_params& p, int rows, int S, const float* o_part,
                               const float* lse_part, void* o, float* lse, cudaStream_t st);
 
+// kv8.cu: the FP8 KV rows (608 bytes) an attention call reads, widened to bfloat16
+// rows in the workspace.  With idx (a decode selection, [B, k]) the valid selected
+// entries are packed to the front of a [B, k] list and out->idx = 0, 1, .., -1;
+// without, every entry of the cache [B, n_cap] is widened and out->idx is null.
+struct KvExpanded {
+  const void* ck;
+  const void* cv;
+  int n_cap;
+  const int32_t* idx;
+};
+size_t kv8_expand_bytes(const ha_params& p, int n_cap, bool select);
+cudaError_t launch_kv8_expand(const ha_params& p, const void* ck8, const void* cv8, int n_cap,
+                              const int32_t* idx, const int32_t* ctx_len, void* ws,
+                              KvExpanded* out, cudaStream_t st);
+
 // attention_tc.cu: tcgen05 attention for bf16, d = 512, H a multiple of 64 (decode
 // rows and prefill rows alike; each row has its own key list).
 bool attention_tc_supported(const ha_params& p, int n_cap, int tok_cap);

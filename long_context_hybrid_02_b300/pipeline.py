@@ -39,8 +39,13 @@ class HybridLayer:
         self.tok_cap = tok_cap or tokens["k_tok"].shape[1]
         self.n_cap = n_cap or w.n_blocks
         dt = w.torch_dtype
-        self.ck = torch.empty((w.B, self.n_cap, w.d), dtype=dt, device=device)
-        self.cv = torch.empty((w.B, self.n_cap, w.d), dtype=dt, device=device)
+        self.kv8 = bool(w.fmt & B.FMT_KV8)
+        if self.kv8:                        # 608-byte FP8 rows of the compressed K / V
+            self.ck = torch.empty((w.B, self.n_cap, B.KV8_ROW_BYTES), dtype=torch.uint8, device=device)
+            self.cv = torch.empty((w.B, self.n_cap, B.KV8_ROW_BYTES), dtype=torch.uint8, device=device)
+        else:
+            self.ck = torch.empty((w.B, self.n_cap, w.d), dtype=dt, device=device)
+            self.cv = torch.empty((w.B, self.n_cap, w.d), dtype=dt, device=device)
         self.fp4 = bool(w.fmt & B.FMT_IDX4)
         if not self.csa:
             self.cki = None

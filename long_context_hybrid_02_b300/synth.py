@@ -87,6 +87,13 @@ WORKLOADS["csa_decode_64k_fp4"] = replace(WORKLOADS["csa_decode_64k"], name="csa
                                           fmt=2)
 WORKLOADS["csa_decode_1m_fp4"] = replace(WORKLOADS["csa_decode_1m"], name="csa_decode_1m_fp4",
                                          fmt=2)
+# compressed K/V in the FP8 format (RoPE dims bfloat16, the rest e4m3), and both formats
+WORKLOADS["csa_decode_64k_kv8"] = replace(WORKLOADS["csa_decode_64k"], name="csa_decode_64k_kv8",
+                                          fmt=1)
+WORKLOADS["hca_decode_128k_kv8"] = replace(WORKLOADS["hca_decode_128k"],
+                                           name="hca_decode_128k_kv8", fmt=1)
+WORKLOADS["csa_decode_1m_fp4_kv8"] = replace(WORKLOADS["csa_decode_1m"],
+                                             name="csa_decode_1m_fp4_kv8", fmt=3)
 
 _TENSOR_IDS = {"k_tok": 1, "v_tok": 2, "ki_tok": 3, "gate": 4, "q": 5, "qI": 6, "w": 7,
                "plant": 8, "extra": 9}

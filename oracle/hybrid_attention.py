@@ -59,6 +59,7 @@ import numpy as np
 
 __all__ = [
     "round_to_bf16", "round_to_storage", "round_to_e4m3", "fp8_kv_encode", "fp8_kv_decode",
+    "fp8_kv_pack", "fp8_kv_unpack",
     "round_to_e2m1", "fp4_encode", "fp4_decode", "fp4_pack", "fp4_unpack",
     "gate_softmax", "compress_block",
     "compress", "n_eligible", "window_positions", "index_scores", "topk_select",
@@ -99,7 +100,10 @@ def round_to_storage(x, storage: str):
 # dims) as bfloat16 and stores dims 64..511 as float8 e4m3fn values with one
 # float32 scale per group of 64 dims, scale = max|x| / 448 over the group (so the
 # largest element maps to the largest e4m3 value), codes rounded to nearest,
-# ties to even; a row takes 128 + 448 + 28 = 604 bytes instead of 1,024.
+# ties to even; a row takes 128 + 448 + 28 = 604 bytes instead of 1,024 (stored
+# padded to 608: fp8_kv_pack / fp8_kv_unpack).  As for FP4 below, the decisions
+# (amax / 448 and x / scale) are float32 divisions of the row's float32 values,
+# the precision the kernels take them in.
 # --------------------------------------------------------------------------
 E4M3_MAX = 448.0            # 1.75 * 2**8, the largest finite e4m3fn value
 FP8_ROPE_DIMS = 64
@@ -130,11 +134,34 @@ def fp8_kv_encode(row):
     [448 // 64, 64] as float64 values, float32 scales [448 // 64])."""
     row = np.asarray(row, dtype=np.float64)
     rope = round_to_bf16(row[:FP8_ROPE_DIMS])
-    rest = row[FP8_ROPE_DIMS:].reshape(-1, FP8_GROUP)
-    scale = (np.abs(rest).max(axis=1) / E4M3_MAX).astype(np.float32).astype(np.float64)
-    safe = np.where(scale > 0, scale, 1.0)
-    codes = round_to_e4m3(rest / safe[:, None])
-    codes[scale == 0] = 0.0
+    rest = row[FP8_ROPE_DIMS:].reshape(-1, FP8_GROUP).astype(np.float32)
+    scale32 = (np.abs(rest).max(axis=1) / np.float32(E4M3_MAX)).astype(np.float32)
+    safe = np.where(scale32 > 0, scale32, np.float32(1.0)).astype(np.float32)
+    codes = round_to_e4m3((rest / safe[:, None]).astype(np.float32))
+    codes[scale32 == 0] = 0.0
+    return rope, codes, scale32.astype(np.float64)
+
+
+FP8_ROW_BYTES = 608
+
+
+def fp8_kv_pack(rope, codes, scale):
+    """The stored FP8 row: bytes [0, 128) the RoPE dims as bfloat16, [128, 576) the
+    e4m3fn codes of dims 64..511, [576, 604) the 7 float32 scales, [604, 608) zero."""
+    out = np.zeros(FP8_ROW_BYTES, dtype=np.uint8)
+    r32 = np.asarray(rope, dtype=np.float64).astype(np.float32)     # exact: bf16 values
+    out[:128] = (r32.view(np.uint32) >> 16).astype(np.uint16).view(np.uint8)
+    out[128:576] = _e4m3_bits(np.asarray(codes, dtype=np.float64).reshape(-1))
+    out[576:604] = np.asarray(scale, dtype=np.float64).astype(np.float32).view(np.uint8)
+    return out
+
+
+def fp8_kv_unpack(row):
+    """Inverse of fp8_kv_pack: (rope [64], codes [7, 64], scale [7]) as float64."""
+    row = np.asarray(row, dtype=np.uint8)
+    rope = (row[:128].view(np.uint16).astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    codes = _e4m3_value(row[128:576]).reshape(-1, FP8_GROUP)
+    scale = row[576:604].copy().view(np.float32).astype(np.float64)
     return rope, codes, scale
 
 

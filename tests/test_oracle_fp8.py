@@ -120,3 +120,30 @@ def test_pins_catch_a_scale_for_the_wrong_e4m3_variant(monkeypatch):
     monkeypatch.setattr(H, "E4M3_MAX", 240.0)
     with pytest.raises(AssertionError):
         test_fp8_kv_constant_row()
+
+
+def test_fp8_row_bytes_worked_example_and_round_trip():
+    """The 608-byte row: bf16 RoPE dims, e4m3fn codes, float32 scales, 4 zero bytes."""
+    rope = np.zeros(64)
+    rope[0], rope[63] = 1.0, -2.5                    # bf16 0x3F80, 0xC020
+    codes = np.zeros((7, 64))
+    codes[0, 0], codes[6, 63] = 448.0, -0.75         # e4m3fn 0x7E, 0xB4
+    scale = np.array([1.0, 0.5, 0.0, 2.0 ** -20, 3.0, 1e-3, 7.25])
+    row = O.fp8_kv_pack(rope, codes, scale)
+    assert row.shape == (608,) and row.dtype == np.uint8
+    assert row[0:2].tolist() == [0x80, 0x3F] and row[126:128].tolist() == [0x20, 0xC0]
+    assert row[128] == 0x7E and row[575] == 0xB4 and (row[129:575] == 0).all()
+    assert row[576:580].tolist() == [0, 0, 0x80, 0x3F]          # float32 1.0
+    assert (row[604:] == 0).all()
+    r2, c2, s2 = O.fp8_kv_unpack(row)
+    assert np.array_equal(r2, rope) and np.array_equal(c2, codes)
+    assert np.array_equal(s2, scale.astype(np.float32).astype(np.float64))
+
+
+def test_fp8_pack_round_trips_encoded_rows():
+    rng = np.random.default_rng(12)
+    for _ in range(20):
+        row = rng.standard_normal(512) / math.sqrt(512)
+        enc = O.fp8_kv_encode(row)
+        assert np.array_equal(O.fp8_kv_decode(*O.fp8_kv_unpack(O.fp8_kv_pack(*enc))),
+                              O.fp8_kv_decode(*enc))
