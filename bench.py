@@ -32,7 +32,6 @@ import hashlib
 import json
 import math
 import os
-import re
 import statistics
 import sys
 import time
@@ -192,20 +191,20 @@ def peaks():
 
 def profiled_traffic(workload: str | None, kernel_name: str, source_file: str):
     """DRAM bytes per launch of `kernel_name` in `workload` from the committed ncu
-    summary, or None when there is none or the kernel's source changed since the
-    capture."""
+    table (profiles/dram_traffic.json: a list of {workload, kernel, source, sha256_16,
+    bytes, ...} records), or None when there is none or the kernel's source file no
+    longer has the SHA-256 prefix it had when the counters were taken."""
     if workload is None:
         return None
-    path = os.path.join(ROOT, "profiles", "dram_traffic.md")
+    path = os.path.join(ROOT, "profiles", "dram_traffic.json")
     if not os.path.exists(path):
         return None
     src = os.path.join(ROOT, "long_context_hybrid_02_b300", "csrc", source_file)
     sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
-    for line in open(path):
-        m = re.match(r"\|\s*(\S+)\s*\|\s*(\S+)\s*\|\s*(\S+)\s*\|\s*([0-9.eE+]+)\s*\|"
-                     r"\s*([0-9a-f]{16})\s*\|", line)
-        if m and m.group(1) == workload and m.group(2) == kernel_name and m.group(5) == sha:
-            return float(m.group(4))
+    for rec in json.load(open(path))["records"]:
+        if (rec["workload"] == workload and rec["kernel"] == kernel_name
+                and rec["source"] == source_file and rec["sha256_16"] == sha):
+            return float(rec["bytes"])
     return None
 
 

@@ -95,10 +95,10 @@ def test_traffic_row_applies_only_to_its_workload_kernel_and_source(tmp_path, mo
     (src / "k.cu").write_text("kernel v1\n")
     sha = hashlib.sha256(b"kernel v1\n").hexdigest()[:16]
     (tmp_path / "profiles").mkdir()
-    (tmp_path / "profiles" / "dram_traffic.md").write_text(
-        "| workload | kernel key | source | bytes per launch | source sha256[:16] | note |\n"
-        "|---|---|---|---|---|---|\n"
-        f"| wl_a | attention | k.cu | 12345 | {sha} | x |\n")
+    import json
+    (tmp_path / "profiles" / "dram_traffic.json").write_text(json.dumps({"records": [
+        {"workload": "wl_a", "kernel": "attention", "source": "k.cu", "sha256_16": sha,
+         "bytes": 12345, "note": "x"}]}))
     monkeypatch.setattr(bench, "ROOT", str(tmp_path))
     assert bench.profiled_traffic("wl_a", "attention", "k.cu") == 12345.0
     assert bench.profiled_traffic("wl_b", "attention", "k.cu") is None
