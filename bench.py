@@ -501,11 +501,21 @@ def run_prefill(args, w, dev, world, rank, dist):
     pk = peaks()
     att_tf = attn_flops / (kern_ms["attention"] * 1e-3) / 1e12
     idx_tf = idx_flops / (kern_ms["index"] * 1e-3) / 1e12
-    roofline = {"bound": "tensor", "kernel": "attention", "achieved": round(att_tf, 1),
-                "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
-                "frac": round(att_tf / pk["bf16_tflops"], 4), "traffic": None,
-                "algorithmic_flops": attn_flops,
-                "peak_source": pk["source"] + " (MEASURED_PEAKS.json bf16_tflops, burst)"}
+    # one roofline entry per tensor-core kernel; `roofline` is the one with the larger
+    # share of the step (the indexer on this workload)
+    full_size = args.ctx == 0 and args.batch == 0
+    entries = {}
+    for name, tf, fl, src in (("index", idx_tf, idx_flops, "indexer_tc.cu"),
+                              ("attention", att_tf, attn_flops, "attention_tc.cu")):
+        entries[name] = {
+            "bound": "tensor", "kernel": name, "achieved": round(tf, 1),
+            "peak": pk["bf16_tflops"], "unit": "TFLOP/s", "frac": round(tf / pk["bf16_tflops"], 4),
+            "traffic": profiled_traffic(args.workload if full_size else None, name, src),
+            "algorithmic_flops": fl, "ms": round(kern_ms[name], 5),
+            "peak_source": pk["source"] + " (MEASURED_PEAKS.json bf16_tflops, burst)"}
+    dom = "index" if kern_ms["index"] >= kern_ms["attention"] else "attention"
+    roofline = entries[dom]
+    roofline_other = entries["attention" if dom == "index" else "index"]
 
     # end to end: the chunk's token rows and queries from pinned host memory, outputs back
     h_in = {k: torch.empty_like(qry[k], device="cpu").pin_memory() for k in ("q", "qI", "w_idx")}
@@ -611,6 +621,7 @@ def run_prefill(args, w, dev, world, rank, dist):
                           "beside the next; L2 flushed before every step"},
         "gpu_launches": int(launches_per_step) * args.steps,
         "roofline": roofline,
+        "roofline_" + roofline_other["kernel"]: roofline_other,
         "indexer_tflops": round(idx_tf, 1),
         "indexer_frac_of_sustained": (round(idx_tf / pk["bf16_tflops_sustained"], 4)
                                       if pk.get("bf16_tflops_sustained") else None),
