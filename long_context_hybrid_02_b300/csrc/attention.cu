@@ -176,8 +176,12 @@ __global__ void __launch_bounds__(kThreads) attn_simt(AttnArgs a) {
 }
 
 // o = sum_s exp(lse_s - LSE) o_s, LSE = log sum_s exp(lse_s), splits in order.
-// One CTA per (row, head): the split weights once into shared memory, then 4-dim
-// groups with up to 8 splits' loads in flight before they are combined.
+// One warp per (row, head, slice of dims), kMergeHeads warps per CTA; lane l owns
+// QPL 4-dim groups l, l + 32, .. of its slice (128 * QPL dims).  The splits are
+// taken 16 / QPL at a time with all sixteen loads of a lane in flight, the first
+// group requested before the weights: with few splits (S <= 4, QPL = 4) the
+// partials and the lse values arrive in one round trip; with many (QPL = 1) the
+// dims are spread over more warps and 16 splits arrive per round trip.
 __device__ __forceinline__ void store4(float* o, const float4& v) {
   *reinterpret_cast<float4*>(o) = v;
 }
@@ -189,55 +193,79 @@ __device__ __forceinline__ void store4(__nv_bfloat16* o, const float4& v) {
   *reinterpret_cast<uint2*>(o) = pk;
 }
 
-template <typename T>
-__global__ void __launch_bounds__(128) attn_merge(const float* __restrict__ o_part,
+constexpr int kMergeHeads = 8;
+
+// v[j][u] = split s0 + j, dims c0 + 4 * (lane + 32 u) .. + 3 (zeros past S or d)
+template <int QPL>
+__device__ __forceinline__ void merge_load(float4 (&v)[16 / QPL][QPL], const float* base,
+                                           long long ss, int S, int d, int s0, int c0, int lane) {
+#pragma unroll
+  for (int j = 0; j < 16 / QPL; ++j)
+#pragma unroll
+    for (int u = 0; u < QPL; ++u) {
+      const int c = c0 + 4 * (lane + 32 * u);
+      v[j][u] = (s0 + j < S && c < d)
+                    ? __ldcg(reinterpret_cast<const float4*>(base + (s0 + j) * ss + c))
+                    : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+}
+
+template <typename T, int QPL>
+__global__ void __launch_bounds__(32 * kMergeHeads) attn_merge(const float* __restrict__ o_part,
                                                   const float* __restrict__ lse_part, int S,
                                                   int H, int d, T* __restrict__ o,
                                                   float* __restrict__ lse) {
-  extern __shared__ float wts[];                  // [S]
-  __shared__ float s_inv;
+  constexpr int SPC = 16 / QPL;                   // splits per round trip
+  extern __shared__ float wts[];                  // [kMergeHeads][S]
   pdl_wait_then_release();
-  const int row = blockIdx.x, h = blockIdx.y;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int n_sl = (d + 128 * QPL - 1) / (128 * QPL);
+  const int gw = blockIdx.y * kMergeHeads + warp;
+  const int row = blockIdx.x, h = gw / n_sl, c0 = (gw % n_sl) * (128 * QPL);
+  if (h >= H) return;
+  float* wv = wts + warp * S;
   const float* lp = lse_part + (long long)row * S * H + h;
-  if (threadIdx.x < 32) {
-    float mx = -INFINITY;
-    for (int s = threadIdx.x; s < S; s += 32) mx = fmaxf(mx, lp[(long long)s * H]);
-    mx = warp_max(mx);
-    float tot = 0.f;
-    for (int s = threadIdx.x; s < S; s += 32) {
-      const float w = mx == -INFINITY ? 0.f : expf(lp[(long long)s * H] - mx);
-      wts[s] = w;
-      tot += w;
-    }
-    tot = warp_sum(tot);
-    if (threadIdx.x == 0) {
-      s_inv = tot > 0.f ? 1.f / tot : 0.f;
-      if (lse) lse[(long long)row * H + h] = tot > 0.f ? mx + logf(tot) : -INFINITY;
+  const float* base = o_part + ((long long)row * S * H + h) * d;
+  const long long ss = (long long)H * d;
+  float4 v[SPC][QPL];
+  merge_load<QPL>(v, base, ss, S, d, 0, c0, lane);
+  float mx = -INFINITY;
+  for (int s = lane; s < S; s += 32) mx = fmaxf(mx, __ldcg(lp + (long long)s * H));
+  mx = warp_max(mx);
+  float tot = 0.f;
+  for (int s = lane; s < S; s += 32) {
+    const float w = mx == -INFINITY ? 0.f : expf(__ldcg(lp + (long long)s * H) - mx);
+    wv[s] = w;
+    tot += w;
+  }
+  tot = warp_sum(tot);
+  __syncwarp();
+  const float inv = tot > 0.f ? 1.f / tot : 0.f;
+  if (lane == 0 && lse && c0 == 0) lse[(long long)row * H + h] = tot > 0.f ? mx + logf(tot) : -INFINITY;
+  float4 acc[QPL];
+#pragma unroll
+  for (int u = 0; u < QPL; ++u) acc[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int s0 = 0; s0 < S; s0 += SPC) {
+    if (s0 != 0) merge_load<QPL>(v, base, ss, S, d, s0, c0, lane);
+#pragma unroll
+    for (int j = 0; j < SPC; ++j) {
+      if (s0 + j >= S) break;
+      const float w = wv[s0 + j];
+#pragma unroll
+      for (int u = 0; u < QPL; ++u) {
+        acc[u].x = fmaf(w, v[j][u].x, acc[u].x);
+        acc[u].y = fmaf(w, v[j][u].y, acc[u].y);
+        acc[u].z = fmaf(w, v[j][u].z, acc[u].z);
+        acc[u].w = fmaf(w, v[j][u].w, acc[u].w);
+      }
     }
   }
-  __syncthreads();
-  const float inv = s_inv;
-  const float* base = o_part + ((long long)row * S * H + h) * d;
-  const long long sstride = (long long)H * d;
-  for (int c = 4 * threadIdx.x; c < d; c += 4 * blockDim.x) {
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int s0 = 0; s0 < S; s0 += 8) {
-      float4 v[8];
+  T* orow = o + ((long long)row * H + h) * d;
 #pragma unroll
-      for (int j = 0; j < 8; ++j)
-        if (s0 + j < S) v[j] = __ldcg(reinterpret_cast<const float4*>(base + (s0 + j) * sstride + c));
-#pragma unroll
-      for (int j = 0; j < 8; ++j)
-        if (s0 + j < S) {
-          const float w = wts[s0 + j];
-          acc.x = fmaf(w, v[j].x, acc.x);
-          acc.y = fmaf(w, v[j].y, acc.y);
-          acc.z = fmaf(w, v[j].z, acc.z);
-          acc.w = fmaf(w, v[j].w, acc.w);
-        }
-    }
-    store4(o + ((long long)row * H + h) * d + c,
-           make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv));
+  for (int u = 0; u < QPL; ++u) {
+    const int c = c0 + 4 * (lane + 32 * u);
+    if (c < d)
+      store4(orow + c, make_float4(acc[u].x * inv, acc[u].y * inv, acc[u].z * inv, acc[u].w * inv));
   }
 }
 
@@ -270,20 +298,32 @@ cudaError_t launch_t(const AttnArgs& a, int rows, cudaStream_t st) {
     case 16: e = launch_dpl<T, 16>(a, rows, smem, st); break;
     default: e = launch_dpl<T, 32>(a, rows, smem, st); break;
   }
-  if (e != cudaSuccess || a.n_splits == 1) return e;
-  return launch_pdl(attn_merge<T>, dim3(rows, a.H), dim3(128), a.n_splits * sizeof(float), st, 1,
-                    a.o_part, a.lse_part, a.n_splits, a.H, a.d, static_cast<T*>(a.o), a.lse);
+  return e;
 }
 
 }  // namespace
 
+template <typename T, int QPL>
+cudaError_t launch_merge_t(int rows, int S, int H, int d, const float* o_part, const float* lse_part,
+                           void* o, float* lse, cudaStream_t st) {
+  const int n_sl = (d + 128 * QPL - 1) / (128 * QPL);
+  const dim3 grid(rows, (H * n_sl + kMergeHeads - 1) / kMergeHeads);
+  const size_t smem = size_t(kMergeHeads) * S * sizeof(float);   // up to 128 KiB (S <= 4096)
+  if (smem > 48 * 1024) {
+    const cudaError_t e = ensure_smem(reinterpret_cast<const void*>(attn_merge<T, QPL>), smem);
+    if (e != cudaSuccess) return e;
+  }
+  return launch_pdl(attn_merge<T, QPL>, grid, dim3(32 * kMergeHeads), smem, st, 1, o_part,
+                    lse_part, S, H, d, static_cast<T*>(o), lse);
+}
+
 cudaError_t launch_attn_merge(const ha_params& p, int rows, int S, const float* o_part,
                               const float* lse_part, void* o, float* lse, cudaStream_t st) {
   if (p.dtype == HA_BF16)
-    return launch_pdl(attn_merge<__nv_bfloat16>, dim3(rows, p.H), dim3(128), S * sizeof(float), st,
-                      1, o_part, lse_part, S, p.H, p.d, static_cast<__nv_bfloat16*>(o), lse);
-  return launch_pdl(attn_merge<float>, dim3(rows, p.H), dim3(128), S * sizeof(float), st, 1,
-                    o_part, lse_part, S, p.H, p.d, static_cast<float*>(o), lse);
+    return S <= 4 ? launch_merge_t<__nv_bfloat16, 4>(rows, S, p.H, p.d, o_part, lse_part, o, lse, st)
+                  : launch_merge_t<__nv_bfloat16, 1>(rows, S, p.H, p.d, o_part, lse_part, o, lse, st);
+  return S <= 4 ? launch_merge_t<float, 4>(rows, S, p.H, p.d, o_part, lse_part, o, lse, st)
+                : launch_merge_t<float, 1>(rows, S, p.H, p.d, o_part, lse_part, o, lse, st);
 }
 
 AttnPlan plan_attention_simt(const ha_params& p, int rows, int max_keys, bool decode) {
@@ -329,7 +369,10 @@ cudaError_t launch_attention_simt(const ha_params& p, const AttnPlan& pl, int de
     a.o_part = static_cast<float*>(ws);
     a.lse_part = a.o_part + size_t(rows) * pl.n_splits * p.H * p.d;
   }
-  return p.dtype == HA_BF16 ? launch_t<__nv_bfloat16>(a, rows, st) : launch_t<float>(a, rows, st);
+  const cudaError_t e =
+      p.dtype == HA_BF16 ? launch_t<__nv_bfloat16>(a, rows, st) : launch_t<float>(a, rows, st);
+  if (e != cudaSuccess || a.n_splits == 1) return e;
+  return launch_attn_merge(p, rows, a.n_splits, a.o_part, a.lse_part, a.o, a.lse, st);
 }
 
 }  // namespace ha

@@ -78,22 +78,26 @@ def test_sharded_decode_matches_the_oracle(name, G, ctx):
     assert_lse_close(np64(lse), rl, w.dtype, "lse")
 
 
-def test_merge_call_against_the_oracle_merge():
+@pytest.mark.parametrize("rows,S_,H,d,dt", [(3, 5, 64, 512, "f32"), (2, 3, 64, 512, "bf16"),
+                                             (2, 1700, 10, 136, "bf16"), (1, 37, 9, 1024, "f32")])
+def test_merge_call_against_the_oracle_merge(rows, S_, H, d, dt):
     """hybrid_attn_merge on random partials (some without keys) against the oracle's
-    merge_partials."""
-    rows, S_, H, d = 3, 5, 64, 512
+    merge_partials: head counts that do not fill a CTA's heads, head dims that do
+    not fill a 512-dim pass, split counts past one group of four and past the
+    default shared-memory limit (1,700 splits)."""
     g = torch.Generator(device=DEV).manual_seed(3)
     o_part = torch.randn((rows, S_, H, d), generator=g, device=DEV)
     lse_part = torch.randn((rows, S_, H), generator=g, device=DEV) * 4
-    lse_part[1, 2] = float("-inf")
-    lse_part[2, :, 5] = float("-inf")            # a head with no key in any part
-    p = B.make_params(rows, H, d, 128, 4, dtype=B.F32)
-    o = torch.empty((rows, H, d), device=DEV)
+    last = min(rows - 1, 2)
+    lse_part[min(rows - 1, 1), 2] = float("-inf")    # a split without keys
+    lse_part[last, :, 5] = float("-inf")             # a head with no key in any part
+    p = B.make_params(rows, H, d, 128, 4, dtype=B.F32 if dt == "f32" else B.BF16)
+    o = torch.empty((rows, H, d), device=DEV, dtype=torch.float32 if dt == "f32" else torch.bfloat16)
     lse = torch.empty((rows, H), device=DEV)
     B.hybrid_attn_merge(p, rows, S_, o_part, lse_part, o, lse)
     torch.cuda.synchronize()
     for r in range(rows):
         ro, rl = O.merge_partials(np64(o_part[r]), np64(lse_part[r]))
-        assert_close(np64(o[r]), ro, "f32", f"o[{r}]")
+        assert_close(np64(o[r]), ro, dt, f"o[{r}]")
         assert_lse_close(np64(lse[r]), rl, "f32", f"lse[{r}]")
-    assert (np64(o[2, 5]) == 0).all() and np.isneginf(np64(lse[2, 5]))
+    assert (np64(o[last, 5]) == 0).all() and np.isneginf(np64(lse[last, 5]))
