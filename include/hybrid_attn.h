@@ -346,6 +346,19 @@ int32_t ha_abi_version(void);
  * launches recorded into a CUDA graph count once, at capture). */
 uint64_t ha_launch_count(void);
 
+/* Page-locked host memory for staging a step's inputs and outputs (not part of
+ * the method): `bytes` (> 0) bytes from cudaHostAlloc, owned by the caller and
+ * released with ha_host_free.  write_combined != 0 asks for write-combined memory
+ * (fast host writes and device reads; host reads are slow: use it for inputs
+ * only).  Copies from this memory to the device reach the link's bandwidth,
+ * which memory registered after allocation may not.  Returns NULL on failure
+ * (ha_last_error says why). */
+void* ha_host_alloc(size_t bytes, int32_t write_combined);
+
+/* Release memory from ha_host_alloc (NULL is a no-op).  HA_ERR_CUDA when the
+ * runtime refuses. */
+ha_status ha_host_free(void* p);
+
 #ifdef __cplusplus
 }
 #endif

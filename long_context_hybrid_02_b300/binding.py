@@ -69,7 +69,8 @@ _SIGS = {
     "ha_device_error": [ctypes.POINTER(ctypes.c_int32), _I],
     "ha_selftest_wait_timeout": [_I, _P],
 }
-EXPORTS = list(_SIGS) + ["ha_status_string", "ha_last_error", "ha_abi_version", "ha_launch_count"]
+EXPORTS = list(_SIGS) + ["ha_status_string", "ha_last_error", "ha_abi_version", "ha_launch_count",
+                         "ha_host_alloc", "ha_host_free"]
 
 _lib = None
 
@@ -94,6 +95,10 @@ def load_library(path: str = LIB_PATH):
     lib.ha_abi_version.restype = ctypes.c_int32
     lib.ha_launch_count.argtypes = []
     lib.ha_launch_count.restype = ctypes.c_uint64
+    lib.ha_host_alloc.argtypes = [ctypes.c_size_t, ctypes.c_int32]
+    lib.ha_host_alloc.restype = ctypes.c_void_p
+    lib.ha_host_free.argtypes = [ctypes.c_void_p]
+    lib.ha_host_free.restype = ctypes.c_int
     _lib = lib
     return lib
 
@@ -217,6 +222,25 @@ def ha_abi_version() -> int:
 
 def ha_launch_count() -> int:
     return load_library().ha_launch_count()
+
+
+def host_empty(shape, dtype, write_combined: bool = False):
+    """A CPU tensor of `shape` and `dtype` in page-locked memory from ha_host_alloc
+    (released when the last tensor viewing it is gone).  Copies between it and the
+    device run at the link's bandwidth; write_combined for inputs the host only
+    writes."""
+    import math
+    import weakref
+
+    import torch
+    lib = load_library()
+    nbytes = max(1, math.prod(shape)) * torch.empty((), dtype=dtype).element_size()
+    ptr = lib.ha_host_alloc(nbytes, 1 if write_combined else 0)
+    if not ptr:
+        raise MemoryError(f"ha_host_alloc({nbytes}): {lib.ha_last_error().decode()}")
+    buf = (ctypes.c_uint8 * nbytes).from_address(ptr)
+    weakref.finalize(buf, lib.ha_host_free, ptr)
+    return torch.frombuffer(buf, dtype=torch.uint8).view(dtype).reshape(shape)
 
 
 def ha_device_error(clear: bool = True) -> int:

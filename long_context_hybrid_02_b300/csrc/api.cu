@@ -265,6 +265,30 @@ int32_t ha_abi_version(void) { return 3; }
 
 uint64_t ha_launch_count(void) { return ha::launch_count(); }
 
+void* ha_host_alloc(size_t bytes, int32_t write_combined) {
+  g_last_error[0] = 0;
+  if (bytes == 0) {
+    ha::set_last_error("ha_host_alloc: bytes = 0");
+    return nullptr;
+  }
+  void* p = nullptr;
+  const cudaError_t e = cudaHostAlloc(
+      &p, bytes, write_combined ? cudaHostAllocWriteCombined : cudaHostAllocDefault);
+  if (e != cudaSuccess) {
+    char msg[256];
+    snprintf(msg, sizeof msg, "ha_host_alloc(%zu): %s", bytes, cudaGetErrorString(e));
+    ha::set_last_error(msg);
+    return nullptr;
+  }
+  return p;
+}
+
+ha_status ha_host_free(void* p) {
+  g_last_error[0] = 0;
+  if (p == nullptr) return HA_OK;
+  return cuda_status(cudaFreeHost(p), "ha_host_free");
+}
+
 const char* ha_last_error(void) { return g_last_error; }
 
 const char* ha_status_string(ha_status s) {

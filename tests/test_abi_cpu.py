@@ -35,6 +35,12 @@ def test_every_header_symbol_is_exported(lib):
     assert set(names) == set(B.EXPORTS)
 
 
+def test_host_alloc_refuses_zero_bytes_and_frees_null(lib):
+    assert lib.ha_host_alloc(0, 0) is None
+    assert b"bytes = 0" in lib.ha_last_error()
+    assert lib.ha_host_free(None) == 0
+
+
 def test_version_and_status_strings(lib):
     assert B.ha_abi_version() == 3
     for code in range(6):

@@ -55,3 +55,22 @@ def _run():
     assert B.ha_device_error(clear=False) == 0
     _topk_still_matches_the_oracle()
     assert B.ha_device_error(clear=False) == 0
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("wc", [False, True])
+def test_host_buffers_are_page_locked_and_round_trip(wc):
+    """ha_host_alloc memory as CPU tensors: recognised as pinned, copied to the
+    device and back unchanged (write-combined only for host-written inputs)."""
+    import torch
+    from long_context_hybrid_02_b300 import binding as B
+    h = B.host_empty((3, 1000), torch.bfloat16, write_combined=wc)
+    assert h.is_pinned() and h.shape == (3, 1000) and h.dtype == torch.bfloat16
+    src = torch.randn(3, 1000).to(torch.bfloat16)
+    h.copy_(src)
+    d = torch.empty((3, 1000), dtype=torch.bfloat16, device="cuda")
+    d.copy_(h, non_blocking=True)
+    back = B.host_empty((3, 1000), torch.bfloat16)
+    back.copy_(d, non_blocking=True)
+    torch.cuda.synchronize()
+    assert torch.equal(back, src)
