@@ -44,8 +44,13 @@ template <int QT> struct Cfg {
   // round trip and made them the kernel's tail)
   static constexpr int kQBuf = QT == 1 ? 2 : 1;
   static constexpr int kTmemCols = 2 * N < 32 ? 32 : 2 * N;
+  // epilogue warps: one per TMEM lane quarter, or two (each with half of the
+  // group's queries) when four queries share a tile, so that the drain keeps up
+  // with the MMAs
+  static constexpr int kEpiWarps = QT == 4 ? 8 : 4;
+  static constexpr int kThreadsQ = 64 + 32 * kEpiWarps;
   static constexpr size_t kSmem = 1024 + size_t(kStages) * kTileBytes + size_t(kQBuf) * kQBytes +
-                                  4 * QT * kHeads * sizeof(float) + 256;
+                                  size_t(kEpiWarps) * QT * kHeads * sizeof(float) + 256;
 };
 
 static_assert(Cfg<1>::kSmem <= 232448 && Cfg<4>::kSmem <= 232448, "shared-memory budget");
@@ -135,7 +140,7 @@ struct TileWalk {
 };
 
 template <int QT>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(Cfg<QT>::kThreadsQ, 1)
     index_scores_tc(const __grid_constant__ CUtensorMap map_k,
                     const __grid_constant__ CUtensorMap map_q, IdxArgs a) {
   using C = Cfg<QT>;
@@ -146,8 +151,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   unsigned char* s_k = base;                                   // kStages x 32 KiB
   unsigned char* s_q = s_k + size_t(C::kStages) * kTileBytes;  // kQBuf x QT x 16 KiB
-  float* s_w = reinterpret_cast<float*>(s_q + size_t(C::kQBuf) * C::kQBytes);  // [4][QT][64]
-  uint64_t* bars = reinterpret_cast<uint64_t*>(s_w + 4 * QT * kHeads);
+  float* s_w = reinterpret_cast<float*>(s_q + size_t(C::kQBuf) * C::kQBytes);  // [epi warps][QT][64]
+  uint64_t* bars = reinterpret_cast<uint64_t*>(s_w + C::kEpiWarps * QT * kHeads);
   uint64_t* full = bars;                   // [kStages]
   uint64_t* empty = full + C::kStages;     // [kStages]
   uint64_t* acc_full = empty + C::kStages; // [2]
@@ -163,7 +168,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::kStages; ++s) { tc::mbar_init(&full[s], 1); tc::mbar_init(&empty[s], 1); }
-    for (int i = 0; i < 2; ++i) { tc::mbar_init(&acc_full[i], 1); tc::mbar_init(&acc_empty[i], 4); }
+    for (int i = 0; i < 2; ++i) {
+      tc::mbar_init(&acc_full[i], 1);
+      tc::mbar_init(&acc_empty[i], C::kEpiWarps);
+    }
     for (int i = 0; i < C::kQBuf; ++i) { tc::mbar_init(&q_full[i], 1); tc::mbar_init(&q_empty[i], 1); }
     tc::fence_mbar_init();
   }
@@ -239,10 +247,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       } while (walk.next(a));
     }
   } else {
-    // ------------------------------------------------------------ epilogue (warps 2..5)
+    // ------------------------------------------------------------ epilogue (warps 2..)
     const int quarter = warp & 3;                     // TMEM lanes 32*quarter ..
     const int row = quarter * 32 + lane;              // entry within the tile
     float* w_mine = s_w + (warp - 2) * QT * kHeads;   // this warp's copy of the weights
+    // the group's queries this warp drains: all, or one half with two warps per quarter
+    constexpr int QW = C::kEpiWarps == 8 ? QT / 2 : QT;
+    const int qw0 = C::kEpiWarps == 8 ? ((warp - 2) >> 2) * QW : 0;
     int ne_q[QT];                                     // eligible entries of the group's queries
     float w_reg[QT == 1 ? kHeads : 1];                // decode: the weights stay in registers
     int i = 0, prev_g = -1;
@@ -285,16 +296,33 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (j < ne_q[0]) a.scores[((long long)b * a.Tq + q0) * a.n_cap + j] = s;
       } else {
 #pragma unroll
-        for (int q = 0; q < QT; ++q) {
+        for (int qq = 0; qq < QW; ++qq) {
+          const int q = qw0 + qq;
+          const uint32_t col = tmem + (uint32_t(quarter * 32) << 16) + acc * C::N + q * kHeads;
+          float v0[32], v1[32];
+          tc::tmem_ld32x2(col, col + 32, v0, v1);
+          const float4* w4 = reinterpret_cast<const float4*>(w_mine + q * kHeads);
           float s = 0.f;
 #pragma unroll
-          for (int half = 0; half < 2; ++half) {
-            float v[32];
-            tc::tmem_ld32(tmem + (uint32_t(quarter * 32) << 16) + acc * C::N + q * kHeads + half * 32, v);
-#pragma unroll
-            for (int h = 0; h < 32; ++h) s = fmaf(w_mine[q * kHeads + half * 32 + h], fmaxf(v[h], 0.f), s);
+          for (int h4 = 0; h4 < 8; ++h4) {
+            const float4 wv = w4[h4];
+            s = fmaf(wv.x, fmaxf(v0[4 * h4], 0.f), s);
+            s = fmaf(wv.y, fmaxf(v0[4 * h4 + 1], 0.f), s);
+            s = fmaf(wv.z, fmaxf(v0[4 * h4 + 2], 0.f), s);
+            s = fmaf(wv.w, fmaxf(v0[4 * h4 + 3], 0.f), s);
           }
-          if (j < ne_q[q]) a.scores[((long long)b * a.Tq + q0 + q) * a.n_cap + j] = s;
+#pragma unroll
+          for (int h4 = 0; h4 < 8; ++h4) {
+            const float4 wv = w4[8 + h4];
+            s = fmaf(wv.x, fmaxf(v1[4 * h4], 0.f), s);
+            s = fmaf(wv.y, fmaxf(v1[4 * h4 + 1], 0.f), s);
+            s = fmaf(wv.z, fmaxf(v1[4 * h4 + 2], 0.f), s);
+            s = fmaf(wv.w, fmaxf(v1[4 * h4 + 3], 0.f), s);
+          }
+          int ne = ne_q[0];                           // ne_q[q] without a local-memory index
+#pragma unroll
+          for (int x = 1; x < QT; ++x) ne = q == x ? ne_q[x] : ne;
+          if (j < ne) a.scores[((long long)b * a.Tq + q0 + q) * a.n_cap + j] = s;
         }
       }
       tc::fence_before_sync();
@@ -631,7 +659,7 @@ cudaError_t launch_qt(const ha_params& p, const void* q_idx, const float* w_idx,
   }
   IdxArgs a{w_idx, q_pos, static_cast<float*>(scores), p.B, Tq, n_cap, p.n_win, p.m, p.elig, err,
             so.pos_off, so.wait_last};
-  return launch_pdl(index_scores_tc<QT>, dim3(g_num_sms), dim3(kThreads), C::kSmem, st, 1, map_k,
+  return launch_pdl(index_scores_tc<QT>, dim3(g_num_sms), dim3(C::kThreadsQ), C::kSmem, st, 1, map_k,
                     map_q, a);
 }
 
