@@ -239,6 +239,35 @@ def host_buffer_like(t, inputs: bool):
     return B.host_empty(tuple(t.shape), t.dtype, write_combined=inputs)
 
 
+def fp4_indexer_recall(w, tok, qry, layer, dev) -> dict:
+    """Diagnostic (untimed, not a gate): share of the bfloat16 indexer's selection
+    (bf16 keys, float32 scores) that the FP4 indexer (FP4 keys and queries,
+    bfloat16 scores) also selects, on the same tokens and queries, per row, mean
+    and minimum."""
+    import torch
+    from long_context_hybrid_02_b300 import binding as B
+    from long_context_hybrid_02_b300.pipeline import HybridLayer
+    ref = HybridLayer(w.scaled(fmt=0), tok, dev)
+    ref.build_cache()
+    out = {}
+    for name, lay in (("bf16", ref), ("fp4", layer)):
+        B.csa_index_scores(lay.p, qry["qI"], qry["w_idx"], lay.cki, lay.n_cap, qry["q_pos"], 1,
+                           lay.scores)
+        B.csa_topk(lay.p, lay.scores, lay.n_cap, qry["q_pos"], 1, lay.idx,
+                   (lay.ws.data_ptr(), lay.ws.numel()))
+        out[name] = lay.idx.reshape(w.B, -1).cpu().numpy()
+    torch.cuda.synchronize()
+    del ref
+    torch.cuda.empty_cache()
+    rec = []
+    for b in range(w.B):
+        a = set(int(i) for i in out["bf16"][b] if i >= 0)
+        f = set(int(i) for i in out["fp4"][b] if i >= 0)
+        rec.append(len(a & f) / max(1, len(a)))
+    return {"mean": round(sum(rec) / len(rec), 4), "min": round(min(rec), 4), "rows": len(rec),
+            "against": "bfloat16 indexer keys with float32 scores on the same inputs"}
+
+
 def bulk_compress_rate(w, layer, dev, reps: int = 3) -> dict:
     """The cache build (every complete block of every sequence compressed in one
     call), timed with CUDA events after an L2 flush: algorithmic bytes = the blocks'
@@ -682,6 +711,8 @@ def main():
     layer = HybridLayer(w, tok, dev)
     layer.build_cache()
     bulk = bulk_compress_rate(w, layer, dev)
+    recall = (fp4_indexer_recall(w, tok, qry, layer, dev)
+              if w.kind == "csa" and w.fmt & 2 else None)
     new_blk = torch.full((w.B,), (w.L // w.m) - 1 if w.L % w.m == 0 else -1, dtype=torch.int32,
                          device=dev)
     q = qry["q"][:, 0].contiguous()
@@ -948,6 +979,7 @@ def main():
         "cpu_baseline": cpu,
         "kernel_ms": {k: round(v, 5) for k, v in kern_ms.items()},
         "bulk_compress": bulk,
+        "indexer_recall": recall,
         "ms_per_step_with_kernel_events": round(sum(tot_marked) / len(tot_marked), 5),
         "step_algorithmic_gbs": round(sum(nbytes.values()) / (step_ms * 1e-3) / 1e9, 1),
         "wall_s_timed": round(t_wall, 3),
