@@ -568,7 +568,7 @@ def run_prefill(args, w, dev, world, rank, dist):
     d2h = h_out.numel() * h_out.element_size()
     qside = torch.cuda.Stream(device=dev)
     oside = torch.cuda.Stream(device=dev)
-    n_sub = 4 if w.B == 1 and w.Tq % 4 == 0 else 1      # attention sub-chunks (B = 1: contiguous)
+    n_sub = 8 if w.B == 1 and w.Tq % 8 == 0 else 1      # attention sub-chunks (B = 1: contiguous)
     sub = w.Tq // n_sub
     qfork = torch.cuda.Event()
     q_ready = [torch.cuda.Event() for _ in range(n_sub)]
@@ -577,12 +577,19 @@ def run_prefill(args, w, dev, world, rank, dist):
 
     def e2e_step():
         """The chunk through the public API with its host copies, as one graph.  The
-        indexer's inputs are copied first; scoring and selection run over the whole
-        chunk; the attention runs in sub-chunks of queries (the same call on a range
-        of rows), each starting once its part of q has arrived (q is copied on a
-        branch of its own from the start) and each sending its part of o back on
-        another branch while the next sub-chunk computes."""
+        chunk's token rows and the indexer's inputs are copied first; scoring and
+        selection run over the whole chunk; the attention runs in sub-chunks of
+        queries (the same call on a range of rows), each starting once its part of
+        q has arrived (q is copied on a branch of its own right after the indexer's
+        inputs) and each sending its part of o back on another branch while the
+        next sub-chunk computes."""
         s = stream.cuda_stream
+        for k in tok_names:
+            tok[k][:, L0:w.L].copy_(h_in["chunk_" + k], non_blocking=True)
+        for k in ("qI", "w_idx"):
+            qry[k].copy_(h_in[k], non_blocking=True)
+        # q follows the indexer's inputs on the link, so that scoring starts as soon
+        # as they are in (together they would share the link's bandwidth)
         qfork.record(stream)
         qside.wait_event(qfork)
         with torch.cuda.stream(qside):
@@ -590,11 +597,7 @@ def run_prefill(args, w, dev, world, rank, dist):
                 qry["q"][:, c * sub:(c + 1) * sub].copy_(h_in["q"][:, c * sub:(c + 1) * sub],
                                                          non_blocking=True)
                 q_ready[c].record(qside)
-        for k in tok_names:
-            tok[k][:, L0:w.L].copy_(h_in["chunk_" + k], non_blocking=True)
         layer.compress(blk_chunk, n_blk_chunk, s)
-        for k in ("qI", "w_idx"):
-            qry[k].copy_(h_in[k], non_blocking=True)
         B.csa_index_scores(layer.p, qry["qI"], qry["w_idx"], layer.cki, layer.n_cap, qry["q_pos"],
                            w.Tq, layer.scores, s)
         B.csa_topk(layer.p, layer.scores, layer.n_cap, qry["q_pos"], w.Tq, layer.idx, ws, s)
@@ -654,8 +657,9 @@ def run_prefill(args, w, dev, world, rank, dist):
                 "timing": "per step: pinned-host copies of the chunk's token rows (K, V, indexer "
                           "keys, gates) and queries, the step (compression of the blocks the "
                           "chunk completes first) and the copy of o back, one graph between "
-                          "CUDA events; q copied beside compression, scoring and selection, "
-                          "attention in 4 sub-chunks of queries whose outputs are copied back "
+                          "CUDA events; q copied after the indexer's inputs, beside "
+                          "compression, scoring and selection, "
+                          "attention in 8 sub-chunks of queries whose outputs are copied back "
                           "beside the next; L2 flushed before every step"},
         "gpu_launches": int(launches_per_step) * args.steps,
         "roofline": roofline,
