@@ -896,16 +896,18 @@ def main():
         graph: the packed small inputs are copied first on the main stream, then
         the newest token's rows are put into the per-token caches on a side branch
         ahead of the compression that reads them (the attention waits for them: the
-        window holds the newest token); q is copied on a branch of its own beside
-        scoring and selection; o is copied back at the end."""
+        window holds the newest token); q is copied after the packed inputs on a
+        branch of its own, beside scoring and selection; o is copied back at the
+        end."""
         s = stream.cuda_stream
-        qfork.record(stream)
-        qside.wait_event(qfork)
+        d_pack.copy_(h_pack, non_blocking=True)
+        pack_ready.record(stream)
+        # q follows the packed inputs on the link (together they would share its
+        # bandwidth and delay scoring)
+        qside.wait_event(pack_ready)
         with torch.cuda.stream(qside):
             q.copy_(h_q, non_blocking=True)
         qjoin.record(qside)
-        d_pack.copy_(h_pack, non_blocking=True)
-        pack_ready.record(stream)
         side.wait_event(pack_ready)
         with torch.cuda.stream(side):
             for kname in tok_names:
