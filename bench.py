@@ -726,10 +726,10 @@ def main():
     ev = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(n_ev)]
 
     side = torch.cuda.Stream(device=dev)
-    fork, join = torch.cuda.Event(), torch.cuda.Event()
+    join = torch.cuda.Event()
     # Under the disjoint rule with n_win >= m the newest complete block lies inside
-    # the query's window and is not eligible, so its compression can run beside
-    # index / top-k / attention.
+    # the query's window and is not eligible, so in the end-to-end step its
+    # compression runs beside index / top-k / attention.
     concurrent_compress = layer.p.elig == B.ELIG_DISJOINT and w.n_win >= w.m
 
     def step(marks: bool):
@@ -746,33 +746,21 @@ def main():
             layer.decode_step_fused(q, qry["ctx_len"], qry.get("qI"), qry.get("w_idx"), s)
             ev[n_ev - 1].record(stream)
             return
-        overlap = concurrent_compress and not marks
-        if not overlap:
-            layer.compress(new_blk, 1, s)
-        else:
-            fork.record(stream)
-            side.wait_event(fork)
-            layer.compress(new_blk, 1, side.cuda_stream)
-            join.record(side)
-        if marks:
-            ev[1].record(stream)
+        layer.compress(new_blk, 1, s)
+        ev[1].record(stream)
         if w.kind == "csa":
             B.csa_index_scores(layer.p, qry["qI"], qry["w_idx"], layer.cki, layer.n_cap,
                                qry["q_pos"], 1, layer.scores, s)
-            if marks:
-                ev[2].record(stream)
+            ev[2].record(stream)
             B.csa_topk(layer.p, layer.scores, layer.n_cap, qry["q_pos"], 1, layer.idx,
                        (layer.ws.data_ptr(), layer.ws.numel()), s)
-            if marks:
-                ev[3].record(stream)
+            ev[3].record(stream)
             idx = layer.idx
         else:
             idx = None
         B.hybrid_attn_decode(layer.p, q, layer.ck, layer.cv, layer.n_cap, idx, tok["k_tok"],
                              tok["v_tok"], layer.tok_cap, qry["ctx_len"], layer.o, layer.lse,
                              (layer.ws.data_ptr(), layer.ws.numel()), s)
-        if overlap:
-            stream.wait_event(join)
         ev[n_ev - 1].record(stream)
 
     # eager warm-up (sets kernel attributes), then capture both graphs
@@ -887,7 +875,7 @@ def main():
     h2d = total + h_q.numel() * h_q.element_size()
     d2h = h_out.numel() * h_out.element_size()
     qside = torch.cuda.Stream(device=dev)
-    qfork, qjoin, tok_ready = torch.cuda.Event(), torch.cuda.Event(), torch.cuda.Event()
+    qjoin, tok_ready = torch.cuda.Event(), torch.cuda.Event()
     pack_ready = torch.cuda.Event()
     tok_names = [kname for kname in small if kname.startswith("new_")]
 
